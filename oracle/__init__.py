@@ -1,0 +1,130 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention forward.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` are the only permitted users. The
+product library never imports, links or calls anything here, and this package
+imports nothing from the product package.
+
+The arithmetic lives in ``attn_ref.c`` (plain C, fp64, one thread per slice of
+rows); this module only compiles it with gcc and marshals numpy arrays.
+
+Parity status of each function (see the pins in ``tests/test_oracle_pins.py``):
+  attn_ref / attn_ref_rows -- pinned (closed forms, invariants, brute force,
+  an independent library routine, and mutation tests).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_LIB = os.path.join(_HERE, "libattn_ref.so")
+
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle with gcc (strict IEEE fp64: no fast-math)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + ".tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.attn_ref_fwd_rows_f64.argtypes = [
+        u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
+        i64p, i64, f64p, f64p, ctypes.c_int]
+    lib.attn_ref_fwd_rows_f64.restype = ctypes.c_int
+    lib.attn_ref_fwd_f64.argtypes = [
+        u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
+        f64p, f64p, ctypes.c_int]
+    lib.attn_ref_fwd_f64.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        build()
+        _lib = _declare(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _as_bits(x) -> np.ndarray:
+    """Accept uint16 bf16 bit patterns (numpy) or a torch bfloat16 tensor."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint16:
+            raise TypeError("oracle inputs are bf16 bit patterns (numpy uint16)")
+        return np.ascontiguousarray(x)
+    # torch tensor (CPU, bfloat16): reinterpret the bits without arithmetic
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs must be bfloat16")
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def attn_ref_rows(q, k, v, causal: bool, window: int, scale: float, rows=None,
+                  nthreads: int | None = None, lib=None):
+    """fp64 O and LSE for the listed flat rows ((b*Hq)+hq)*N + i (all rows if None).
+
+    q: [B,Hq,N,d], k/v: [B,Hkv,N,d] bf16. Returns (o [nrows,d] f64, lse [nrows] f64).
+    """
+    qb, kb, vb = _as_bits(q), _as_bits(k), _as_bits(v)
+    B, Hq, N, d = qb.shape
+    Hkv = kb.shape[1]
+    if kb.shape != (B, Hkv, N, d) or vb.shape != kb.shape:
+        raise ValueError("k and v must be [B,Hkv,N,d] matching q")
+    if rows is None:
+        nrows = B * Hq * N
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    L = lib or load()
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = L.attn_ref_fwd_rows_f64(
+        qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p),
+        B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+        rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
+        nrows, o.ctypes.data_as(f64p), lse.ctypes.data_as(f64p),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return o, lse
+
+
+def attn_ref(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
+             nthreads: int | None = None, lib=None):
+    """fp64 O [B,Hq,N,d] and LSE [B,Hq,N] for every row."""
+    qb = _as_bits(q)
+    B, Hq, N, d = qb.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    o, lse = attn_ref_rows(qb, k, v, causal, window, scale, None, nthreads, lib)
+    return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)

@@ -1,0 +1,207 @@
+/*
+ * Oracle: exact scaled-dot-product attention forward, computed in fp64 on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call this
+ * file. Its users are the test suite, the smoke check and the CPU-baseline leg of the
+ * benchmark. It shares no code, header, table or constant with the CUDA library.
+ *
+ * What it computes (the plain definition, no tiling, no online softmax):
+ *
+ *   For every batch b, query head hq and query row i:
+ *     kv     = hq / (Hq / Hkv)                     grouped-query head map
+ *     J(i)   = { j in [0,N) : (!causal || j <= i) && (window == 0 || i - j < window) }
+ *     s_ij   = scale * sum_c q[b,hq,i,c] * k[b,kv,j,c]        for j in J(i)
+ *     m_i    = max_j s_ij
+ *     lse_i  = m_i + ln( sum_j exp(s_ij - m_i) )             natural-log log-sum-exp
+ *     o[b,hq,i,c] = sum_j exp(s_ij - lse_i) * v[b,kv,j,c]
+ *
+ * Sources, by page and section:
+ *   - score = QK^T / sqrt(D) and Attention = Softmax(score) V: the SpAtten review
+ *     (coolstone2000.github.io), "Background - Attention Mechanism" formulas.
+ *   - probability p_i = exp(s_i) / sum_j exp(s_j): same page, "Progressive
+ *     Quantization" (attention probability equation).
+ *   - scaling by sqrt(d_k), softmax, weighted sum of V; multi-head as independent
+ *     heads; the look-ahead mask lets a token attend to itself and earlier tokens:
+ *     palettepath-it.com self-attention guide, sections "어텐션 스코어 계산과 스케일링
+ *     닷 프로덕트", "소프트맥스 정규화와 가중치 합산", "병렬 어텐션 헤드의 동작 원리",
+ *     "룩어헤드 마스킹 (Look-Ahead Masking)".
+ *   - grouped-query attention and sliding-window attention are named as compared
+ *     variants on the "Attentions Under the Microscope" summary (gist.science),
+ *     section "방법론". The head map kv = hq / G (consecutive groups) and the window
+ *     rule i - j < window are the plainest readings; the pages fix neither.
+ *
+ * Inputs are bf16 bit patterns (uint16); each is widened exactly to fp64.
+ * A row whose visible set is empty (impossible for valid arguments, since j = i is
+ * always visible) yields o = 0 and lse = -inf.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int key_visible(int64_t i, int64_t j, int causal, int64_t window) {
+    if (causal && j > i) return 0;
+    if (window > 0 && i - j >= window) return 0;
+    return 1;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    int64_t B, Hq, Hkv, N, d;
+    int causal;
+    int64_t window;
+    double scale;
+    const int64_t *rows; /* flat row ids ((b*Hq)+hq)*N + i, or NULL for all rows */
+    int64_t row_begin, row_end;
+    double *o, *lse;     /* o: one d-vector per requested row; lse: one per row */
+} job_t;
+
+/* One query row, straight from the definition above. */
+static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_out,
+                    double *qd, double *s) {
+    const int64_t N = jb->N, d = jb->d;
+    const int64_t i = flat % N;
+    const int64_t bh = flat / N;
+    const int64_t hq = bh % jb->Hq;
+    const int64_t b = bh / jb->Hq;
+    const int64_t group = jb->Hq / jb->Hkv;
+    const int64_t kv = hq / group;
+
+    const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;
+    const uint16_t *kbase = jb->k + (b * jb->Hkv + kv) * N * d;
+    const uint16_t *vbase = jb->v + (b * jb->Hkv + kv) * N * d;
+
+    for (int64_t c = 0; c < d; ++c) qd[c] = bf16_bits_to_double(qrow[c]);
+
+    /* scores over the visible keys */
+    double m = -INFINITY;
+    int64_t nvis = 0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        const uint16_t *krow = kbase + j * d;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += qd[c] * bf16_bits_to_double(krow[c]);
+        s[j] = jb->scale * dot;
+        if (s[j] > m) m = s[j];
+        ++nvis;
+    }
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (nvis == 0) {
+        *lse_out = -INFINITY;
+        return;
+    }
+
+    /* log-sum-exp */
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        l += exp(s[j] - m);
+    }
+    const double lse = m + log(l);
+    *lse_out = lse;
+
+    /* probability-weighted sum of value rows */
+    for (int64_t j = 0; j < N; ++j) {
+        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        const double p = exp(s[j] - lse);
+        const uint16_t *vrow = vbase + j * d;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_bits_to_double(vrow[c]);
+    }
+}
+
+static void *worker(void *arg) {
+    const job_t *jb = (const job_t *)arg;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)jb->d);
+    double *s = (double *)malloc(sizeof(double) * (size_t)jb->N);
+    if (qd && s) {
+        for (int64_t r = jb->row_begin; r < jb->row_end; ++r) {
+            const int64_t flat = jb->rows ? jb->rows[r] : r;
+            one_row(jb, flat, jb->o + r * jb->d, jb->lse + r, qd, s);
+        }
+    }
+    free(qd);
+    free(s);
+    return NULL;
+}
+
+static int check_args(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                      int causal, int64_t window, double scale) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return -3;
+    if (Hq % Hkv != 0) return -3;
+    if (window < 0) return -3;
+    if (window > 0 && !causal) return -4;
+    if (!(scale > 0.0) || !isfinite(scale)) return -3;
+    return 0;
+}
+
+/*
+ * Compute the rows listed in `rows` (flat ids ((b*Hq)+hq)*N + i); when rows is NULL,
+ * compute all B*Hq*N rows in order (nrows must then equal B*Hq*N).
+ * o: nrows * d doubles, lse: nrows doubles. Returns 0, or a negative code for bad
+ * arguments (-1 null pointer, -3 shape, -4 unsupported combination).
+ */
+int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                          int causal, int64_t window, double scale,
+                          const int64_t *rows, int64_t nrows, double *o, double *lse,
+                          int nthreads) {
+    if (!q || !k || !v || !o || !lse) return -1;
+    int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc) return rc;
+    if (nrows < 0) return -3;
+    if (!rows && nrows != B * Hq * N) return -3;
+    if (rows) {
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= B * Hq * N) return -3;
+    }
+    if (nrows == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nrows) nthreads = (int)nrows;
+
+    job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -5;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        job_t *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v;
+        jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d;
+        jb->causal = causal; jb->window = window; jb->scale = scale;
+        jb->rows = rows;
+        jb->row_begin = nrows * t / nthreads;
+        jb->row_end = nrows * (t + 1) / nthreads;
+        jb->o = o; jb->lse = lse;
+    }
+    int spawned = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, worker, &jobs[t]) != 0) break;
+        spawned = t;
+    }
+    worker(&jobs[0]);
+    for (int t = 1; t <= spawned; ++t) pthread_join(tids[t], NULL);
+    /* rows of threads that failed to spawn are done here, serially */
+    for (int t = spawned + 1; t < nthreads; ++t) worker(&jobs[t]);
+    free(jobs);
+    free(tids);
+    return 0;
+}
+
+/* All rows: o is [B,Hq,N,d], lse is [B,Hq,N], both fp64. */
+int attn_ref_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                     int causal, int64_t window, double scale,
+                     double *o, double *lse, int nthreads) {
+    return attn_ref_fwd_rows_f64(q, k, v, B, Hq, Hkv, N, d, causal, window, scale,
+                                 NULL, B * Hq * N, o, lse, nthreads);
+}
