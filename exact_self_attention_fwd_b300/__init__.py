@@ -1,0 +1,14 @@
+"""Exact self-attention forward for B300 (sm_103a): a thin Python binding over the
+C-ABI library libattn_fwd.so (include/attn_api.h). PyTorch supplies device memory
+and streams; the attention itself runs only in the library's CUDA kernel.
+"""
+from ._lib import (ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_NULLPTR, ATTN_ERR_SHAPE,
+                   ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_OK, AttnError, attn_fwd,
+                   attn_fwd_host, device_error, header_functions, load, selftest_wait_timeout,
+                   status_str, version)
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_NULLPTR", "ATTN_ERR_ALIGN", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED",
+    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "AttnError", "attn_fwd", "attn_fwd_host",
+    "device_error", "header_functions", "load", "selftest_wait_timeout", "status_str", "version",
+]

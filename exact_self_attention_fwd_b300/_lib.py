@@ -1,0 +1,182 @@
+"""ctypes binding of libattn_fwd.so: argument marshalling only.
+
+Every step of the attention computation runs in the CUDA library. There is no CPU
+or PyTorch fallback: if the library is missing this module raises, and every call
+refuses tensors that are not CUDA bf16/fp32 of the required shape.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+LIB_PATH = os.path.join(PKG, "libattn_fwd.so")
+HEADER = os.path.join(ROOT, "include", "attn_api.h")
+
+ATTN_OK = 0
+ATTN_ERR_NULLPTR = -1
+ATTN_ERR_ALIGN = -2
+ATTN_ERR_SHAPE = -3
+ATTN_ERR_UNSUPPORTED = -4
+ATTN_ERR_CUDA = -5
+ATTN_ERR_TIMEOUT = -6
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{message} (status {code})")
+        self.code = code
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/attn_api.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+
+
+def _declare(lib):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_fwd_host.restype = i
+    lib.attn_status_str.argtypes = [i]
+    lib.attn_status_str.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error.argtypes = []
+    lib.attn_last_cuda_error.restype = i
+    lib.attn_device_error.argtypes = [i]
+    lib.attn_device_error.restype = i
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_int64]
+    lib.attn_selftest_wait_timeout.restype = i
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = i
+    return lib
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (built in-tree by exact_self_attention_fwd_b300.build)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -m exact_self_attention_fwd_b300.build`"
+                " (there is no fallback implementation)")
+        _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return load().attn_status_str(int(code)).decode()
+
+
+def _check(rc: int):
+    if rc != ATTN_OK:
+        L = load()
+        msg = L.attn_status_str(rc).decode()
+        if rc == ATTN_ERR_CUDA:
+            msg += f"; cudaError {L.attn_last_cuda_error()}"
+        raise AttnError(rc, msg)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensors(q, k, v):
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, d]")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Hq, N, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    return B, Hq, k.shape[1], N, d
+
+
+def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
+             out=None, lse=None, stream=None):
+    """O [B,Hq,N,d] bf16 and LSE [B,Hq,N] fp32 for CUDA bf16 q [B,Hq,N,d], k/v [B,Hkv,N,d].
+
+    Asynchronous on `stream` (default: the current stream of q's device).
+    """
+    import torch
+    B, Hq, Hkv, N, d = _check_tensors(q, k, v)
+    dev = q.device
+    if dev.type != "cuda" or k.device != dev or v.device != dev:
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must be a contiguous bf16 CUDA tensor shaped like q")
+    if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != dev:
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, Hq, N]")
+    L = load()
+    with torch.cuda.device(dev):
+        rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+                        _stream_handle(stream, dev))
+    _check(rc)
+    return out, lse
+
+
+def attn_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, causal: bool = False,
+                  window: int = 0, scale: float | None = None, stream=None):
+    """Host-buffer entry: copies hq/hk/hv into dq/dk/dv, runs, copies do/dlse back into
+    ho/hlse, all queued on `stream`. Host tensors should be pinned; synchronise the
+    stream before reading ho and hlse."""
+    import torch
+    B, Hq, Hkv, N, d = _check_tensors(hq, hk, hv)
+    _check_tensors(dq, dk, dv)
+    dev = dq.device
+    if scale is None:
+        scale = d ** -0.5
+    for t in (hq, hk, hv, ho, hlse):
+        if t.device.type != "cpu":
+            raise ValueError("host buffers must be CPU tensors")
+    for t in (dq, dk, dv, do, dlse):
+        if t.device != dev or dev.type != "cuda":
+            raise ValueError("device buffers must be CUDA tensors on one device")
+    if ho.shape != hq.shape or do.shape != hq.shape or dq.shape != hq.shape or dk.shape != hk.shape:
+        raise ValueError("buffer shapes do not match")
+    if tuple(hlse.shape) != (B, Hq, N) or tuple(dlse.shape) != (B, Hq, N):
+        raise ValueError("lse buffers must be [B, Hq, N]")
+    L = load()
+    with torch.cuda.device(dev):
+        rc = L.attn_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hlse.data_ptr(),
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
+                             B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+                             _stream_handle(stream, dev))
+    _check(rc)
+    return ho, hlse
+
+
+def device_error(clear: bool = True) -> int:
+    """Synchronise and return ATTN_OK or ATTN_ERR_TIMEOUT (see attn_device_error)."""
+    return load().attn_device_error(int(bool(clear)))
+
+
+def selftest_wait_timeout(limit_ns: int) -> int:
+    return load().attn_selftest_wait_timeout(int(limit_ns))
+
+
+def version() -> int:
+    return load().attn_version()

@@ -1,0 +1,825 @@
+// Exact scaled-dot-product attention forward for B300 (sm_103a).
+//
+// What is computed (see include/attn_api.h for the full statement and the pages it
+// follows): O = softmax(scale * Q K^T + mask) V per (batch, query head), with the
+// grouped-query head map kv = hq / (Hq / Hkv), the look-ahead mask j <= i and the
+// causal sliding window i - j < W, plus the natural-log log-sum-exp of every row.
+//
+// How (one persistent kernel, one CTA per SM, 12 warps):
+//   warps 0-3   softmax warpgroup for query tile 0 of the work unit (one row per thread)
+//   warps 4-7   softmax warpgroup for query tile 1
+//   warp 8      TMA producer: Q tiles once per unit, then K_j, V_j through a ring of
+//               shared-memory stages guarded by full/empty mbarriers
+//   warp 9      tensor-memory owner and MMA issuer (one thread): S_t = Q_t K_j^T into
+//               tensor memory, then O_t += P_t V_j with P_t read from tensor memory
+//   warps 10-11 idle; with warps 8-9 they form the warpgroup that hands registers to
+//               the softmax warpgroups (setmaxnreg)
+// A work unit is two consecutive 128-row query tiles of one (batch, query head); both
+// tiles share every K/V tile the unit streams, so each K/V tile staged in shared
+// memory feeds two MMAs. The two softmax warpgroups alternate with the tensor core:
+// while one turns S into P, the tensor core runs the other tile's S and PV products.
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128) S0 / P0   [128,256) S1 / P1   [256,256+D) O0   [256+D,256+2D) O1
+// P (bf16, two per column) overwrites the first half of its S block.
+//
+// Online softmax (the statistics of FlashAttention-2 kept on chip, as the
+// FlashAttention-3 review page describes for FA1/FA2): per row a running maximum m
+// (in log2 units of scale*s) and a running sum l. m is only raised when a tile's row
+// maximum exceeds it by more than 8 (a factor 256), so P <= 256 and O is rescaled
+// rarely; the result is exact because the final normalisation uses the same m.
+//
+// Every mbarrier wait is bounded in time; a wait that runs out sets a device status
+// word, and the kernel drains its own copies and MMAs, frees its tensor memory and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_api.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int BM = 128;  // query rows per tile = tensor-memory lanes
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int NUM_THREADS = 384;  // 3 warpgroups; warps 10-11 only hold registers back
+// Register split: the kernel launches at LAUNCH_REGS per thread; the producer/MMA
+// warpgroup gives registers back and the two softmax warpgroups take them, so that
+// 2 * 128 * SOFTMAX_REGS + 128 * PRODUCER_REGS equals the launch total exactly.
+constexpr int LAUNCH_REGS = 168;
+constexpr int PRODUCER_REGS = 56;
+constexpr int SOFTMAX_REGS = 224;
+static_assert(2 * 128 * SOFTMAX_REGS + 128 * PRODUCER_REGS <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t STATUS_TIMEOUT = 1u;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+constexpr float LN2 = 0.693147180559945309f;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+
+__device__ unsigned int g_status;  // bit 0: some wait ran out of time
+
+struct Params {
+    __nv_bfloat16 *o;
+    float *lse;
+    int B, Hq, Hkv, N, group;
+    int causal, window;
+    int n_pairs, n_kv, num_units;
+    float sl2;  // scale * log2(e)
+    unsigned long long timeout_ns;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int STAGES = (D == 128) ? 4 : 8;
+    static constexpr int CHUNK_BYTES = BM * 64 * 2;  // one 64-column, 128-byte-swizzled slab
+    static constexpr int NCHUNK = D / 64;
+    static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
+    static constexpr int SMEM_Q = 0;
+    static constexpr int SMEM_KV = 2 * TILE_BYTES;
+    static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
+    // barrier indices
+    static constexpr int B_QFULL = 0;               // 2
+    static constexpr int B_QEMPTY = 2;              // 1
+    static constexpr int B_KVFULL = 3;              // STAGES
+    static constexpr int B_KVEMPTY = 3 + STAGES;    // STAGES
+    static constexpr int B_SFULL = 3 + 2 * STAGES;  // 2
+    static constexpr int B_PFULL = B_SFULL + 2;     // 2
+    static constexpr int B_OFULL = B_PFULL + 2;     // 2
+    static constexpr int B_DRAIN = B_OFULL + 2;     // 1
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_TOTAL = SMEM_CTL + 16;
+    static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align to 1024 bytes
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
+};
+
+struct Ctl {
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+
+// ------------------------------------------------------------------ bounded waits
+__device__ __forceinline__ void raise_timeout(volatile uint32_t *abort_flag) {
+    *abort_flag = 1u;
+    atomicOr(&g_status, STATUS_TIMEOUT);
+}
+
+// single-thread wait; false once the limit passes or another role gave up
+__device__ bool wait_one(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                         unsigned long long limit) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > limit) {
+            raise_timeout(abort_flag);
+            return false;
+        }
+    }
+}
+
+// whole-warp wait; every lane returns the same value
+__device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                          unsigned long long limit) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    while (true) {
+        const bool ok = ptx::mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        int give_up = 0;
+        if (lane == 0) {
+            const uint64_t now = ptx::globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            give_up = (*abort_flag != 0u) || (now - t0 > limit);
+        }
+        give_up = __shfl_sync(0xffffffffu, give_up, 0);
+        if (give_up) {
+            if (lane == 0) raise_timeout(abort_flag);
+            return false;
+        }
+    }
+}
+
+// wait for copies in flight on the way out of an aborted run (bounded, no flag)
+__device__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > limit) return;
+    }
+}
+
+// ------------------------------------------------------------------ work units
+// Unit u -> (batch b, query head hq, pair of query tiles). Pairs are visited from
+// the last (the most KV tiles under a causal mask) to the first, so the heavy
+// units start first; consecutive units share the pair index and walk hq fastest,
+// so the G query heads that read one KV head run side by side.
+struct Unit {
+    int b, hq, hkv, pair;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
+    const int BH = p.B * p.Hq;
+    const int pr = u / BH;
+    const int bh = u - pr * BH;
+    Unit w;
+    w.pair = p.n_pairs - 1 - pr;
+    w.b = bh / p.Hq;
+    w.hq = bh - w.b * p.Hq;
+    w.hkv = w.hq / p.group;
+    return w;
+}
+
+// KV tile range [lo, hi) that query tile starting at row q0 must visit; empty when
+// the tile lies past the end of the sequence. Tiles outside the range are fully
+// masked and never loaded.
+__device__ __forceinline__ void tile_range(const Params &p, int q0, int &lo, int &hi) {
+    lo = 0;
+    hi = 0;
+    if (q0 >= p.N) return;
+    // the tile's last row q0 + BM - 1 sees keys up to itself (BM == BN)
+    hi = p.causal ? min(p.n_kv, q0 / BN + 1) : p.n_kv;
+    if (p.causal && p.window > 0) {
+        const int first = q0 - p.window + 1;  // first visible key of row q0
+        lo = first > 0 ? first / BN : 0;
+    }
+}
+
+// a (query tile, key tile) block needs element masking when it crosses the end of
+// the sequence, the causal diagonal or the window edge
+__device__ __forceinline__ bool block_needs_mask(const Params &p, int q0, int kv0) {
+    if (kv0 + BN > p.N) return true;
+    if (p.causal && kv0 + BN - 1 > q0) return true;
+    if (p.window > 0 && (q0 + BM - 1) - kv0 >= p.window) return true;
+    return false;
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sb = raw + pad;
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + C::SMEM_CTL);
+    auto bar = [&](int i) -> uint32_t { return sb + C::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(C::B_QFULL + 0), 1);
+        ptx::mbar_init(bar(C::B_QFULL + 1), 1);
+        ptx::mbar_init(bar(C::B_QEMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar(C::B_KVFULL + s), 1);
+            ptx::mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(C::B_SFULL + t), 1);
+            ptx::mbar_init(bar(C::B_PFULL + t), 4);  // one arrival per softmax warp
+            ptx::mbar_init(bar(C::B_OFULL + t), 1);
+        }
+        ptx::mbar_init(bar(C::B_DRAIN), 1);
+        ctl->abort = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == WARP_TMA && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == WARP_MMA) {
+        ptx::tmem_alloc(sb + C::SMEM_CTL, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile uint32_t *abort_flag = &ctl->abort;
+    const unsigned long long limit = p.timeout_ns;
+
+    if (warp >= 8) {
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        if (warp == WARP_TMA) {
+            // ============================================================ TMA producer
+            if (lane == 0) {
+                uint32_t kv_it = 0, q_it = 0, q_loads0 = 0, q_loads1 = 0;
+                bool ok = true;
+                for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                    const Unit w = decode_unit(u, p);
+                    const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
+                    int lo0, hi0, lo1, hi1;
+                    tile_range(p, q0a, lo0, hi0);
+                    tile_range(p, q0b, lo1, hi1);
+                    const bool has1 = hi1 > lo1;
+                    const int lo = has1 ? min(lo0, lo1) : lo0;
+                    const int hi = has1 ? max(hi0, hi1) : hi0;
+                    const int zq = w.b * p.Hq + w.hq;
+                    const int zkv = w.b * p.Hkv + w.hkv;
+                    ok = wait_one(bar(C::B_QEMPTY), (q_it & 1u) ^ 1u, abort_flag, limit);
+                    ++q_it;
+                    if (!ok) break;
+                    ptx::mbar_arrive_expect_tx(bar(C::B_QFULL + 0), C::TILE_BYTES);
+    #pragma unroll 1
+                    for (int c = 0; c < C::NCHUNK; ++c)
+                        ptx::tma_load_3d(sb + C::SMEM_Q + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 0),
+                                         c * 64, q0a, zq);
+                    ++q_loads0;
+                    if (has1) {
+                        ptx::mbar_arrive_expect_tx(bar(C::B_QFULL + 1), C::TILE_BYTES);
+    #pragma unroll 1
+                        for (int c = 0; c < C::NCHUNK; ++c)
+                            ptx::tma_load_3d(sb + C::SMEM_Q + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
+                                             bar(C::B_QFULL + 1), c * 64, q0b, zq);
+                        ++q_loads1;
+                    }
+                    for (int j = lo; ok && j < hi; ++j) {
+    #pragma unroll 1
+                        for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
+                            const uint32_t s = kv_it % C::STAGES;
+                            const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
+                            if (ok) ok = wait_one(bar(C::B_KVEMPTY + s), ph, abort_flag, limit);
+                            if (ok) {
+                                ptx::mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE_BYTES);
+                                const CUtensorMap *m = kv ? &tm_v : &tm_k;
+    #pragma unroll 1
+                                for (int c = 0; c < C::NCHUNK; ++c)
+                                    ptx::tma_load_3d(sb + C::SMEM_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                                     m, bar(C::B_KVFULL + s), c * 64, j * BN, zkv);
+                                ++kv_it;
+                            }
+                        }
+                    }
+                }
+                if (!ok) {
+                    // let every copy this thread issued land before the CTA exits
+                    for (uint32_t s = 0; s < static_cast<uint32_t>(C::STAGES); ++s) {
+                        if (kv_it <= s) continue;
+                        const uint32_t last = (kv_it - 1u - s) / C::STAGES * C::STAGES + s;
+                        drain_wait(bar(C::B_KVFULL + s), (last / C::STAGES) & 1u, 100000000ull);
+                    }
+                    if (q_loads0) drain_wait(bar(C::B_QFULL + 0), (q_loads0 - 1u) & 1u, 100000000ull);
+                    if (q_loads1) drain_wait(bar(C::B_QFULL + 1), (q_loads1 - 1u) & 1u, 100000000ull);
+                }
+            }
+            __syncwarp();
+        } else if (warp == WARP_MMA) {
+            // ============================================================ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
+                constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
+                uint32_t kv_it = 0, q_use0 = 0, q_use1 = 0, p_use0 = 0, p_use1 = 0;
+                bool ok = true;
+
+                // S_t = Q_t K^T: K-major A and B, 16 columns of d per instruction. The
+                // descriptors of later K steps differ only in the start-address field, so
+                // they are formed by adding the byte offset >> 4 to the first one.
+                auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
+                    const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
+                    const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
+    #pragma unroll 1
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                        ptx::mma_ss(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                };
+                // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory
+                auto issue_pv = [&](uint32_t col_o, uint32_t col_s, uint32_t vslot, bool accumulate) {
+                    const uint64_t vd = ptx::sdesc_sw128(sb + C::SMEM_KV + vslot * C::TILE_BYTES,
+                                                         C::CHUNK_BYTES, 1024);
+    #pragma unroll 1
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        ptx::mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV,
+                                    (accumulate || kk > 0) ? 1u : 0u);
+                    }
+                };
+                const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
+
+                for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                    const Unit w = decode_unit(u, p);
+                    const int q0a = 2 * w.pair * BM;
+                    int lo0, hi0, lo1, hi1;
+                    tile_range(p, q0a, lo0, hi0);
+                    tile_range(p, q0a + BM, lo1, hi1);
+                    const bool has1 = hi1 > lo1;
+                    const int lo = has1 ? min(lo0, lo1) : lo0;
+                    const int hi = has1 ? max(hi0, hi1) : hi0;
+                    ok = wait_one(bar(C::B_QFULL + 0), q_use0 & 1u, abort_flag, limit);
+                    ++q_use0;
+                    if (ok && has1) {
+                        ok = wait_one(bar(C::B_QFULL + 1), q_use1 & 1u, abort_flag, limit);
+                        ++q_use1;
+                    }
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    int prev = -1;
+                    uint32_t vprev = 0, vprev_ph = 0;
+                    for (int j = lo; j < hi; ++j) {
+                        const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        ok = wait_one(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
+                        if (ok && prev >= 0) ok = wait_one(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
+                        if (prev >= lo0 && prev < hi0) {
+                            ok = wait_one(bar(C::B_PFULL + 0), p_use0 & 1u, abort_flag, limit);
+                            ++p_use0;
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_pv(C::COL_O0, C::COL_S0, vprev, prev > lo0);
+                        }
+                        if (j >= lo0 && j < hi0) {
+                            issue_s(qa0, C::COL_S0, ks);
+                            ptx::mma_commit(bar(C::B_SFULL + 0));
+                        }
+                        // tile 1: the same, overlapping softmax of tile 0
+                        if (has1 && prev >= lo1 && prev < hi1) {
+                            ok = wait_one(bar(C::B_PFULL + 1), p_use1 & 1u, abort_flag, limit);
+                            ++p_use1;
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_pv(C::COL_O1, C::COL_S1, vprev, prev > lo1);
+                        }
+                        if (has1 && j >= lo1 && j < hi1) {
+                            issue_s(qa1, C::COL_S1, ks);
+                            ptx::mma_commit(bar(C::B_SFULL + 1));
+                        }
+                        if (prev >= 0) ptx::mma_commit(bar(C::B_KVEMPTY + vprev));
+                        ptx::mma_commit(bar(C::B_KVEMPTY + ks));
+                        prev = j;
+                        vprev = vs;
+                        vprev_ph = vph;
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                    ok = wait_one(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (prev >= lo0 && prev < hi0) {
+                        ok = wait_one(bar(C::B_PFULL + 0), p_use0 & 1u, abort_flag, limit);
+                        ++p_use0;
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_pv(C::COL_O0, C::COL_S0, vprev, prev > lo0);
+                    }
+                    ptx::mma_commit(bar(C::B_OFULL + 0));
+                    if (has1) {
+                        if (prev >= lo1 && prev < hi1) {
+                            ok = wait_one(bar(C::B_PFULL + 1), p_use1 & 1u, abort_flag, limit);
+                            ++p_use1;
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_pv(C::COL_O1, C::COL_S1, vprev, prev > lo1);
+                        }
+                        ptx::mma_commit(bar(C::B_OFULL + 1));
+                    }
+                    ptx::mma_commit(bar(C::B_KVEMPTY + vprev));
+                }
+                // every MMA this thread issued completes before tensor memory is freed
+                ptx::mma_commit(bar(C::B_DRAIN));
+                drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        ptx::setmaxnreg_inc<SOFTMAX_REGS>();
+        // ============================================================ softmax + epilogue
+        const int t = warp >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
+        const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
+        const uint32_t bar_s = bar(C::B_SFULL + t), bar_p = bar(C::B_PFULL + t), bar_o = bar(C::B_OFULL + t);
+        const float sl2 = p.sl2;
+        uint32_t s_use = 0, o_use = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit(u, p);
+            const int q0 = (2 * w.pair + t) * BM;
+            int lo, hi;
+            tile_range(p, q0, lo, hi);
+            if (hi <= lo) continue;
+            const int qi = q0 + row;
+            float m_run = -INFINITY;  // running max of scale*s*log2(e)
+            float l_run = 0.f;        // running sum of 2^(x - m_run)
+            for (int j = lo; j < hi; ++j) {
+                ok = wait_warp(bar_s, s_use & 1u, abort_flag, limit);
+                ++s_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + 32 * c, sr[c]);
+                ptx::tmem_wait_ld();
+                const int kv0 = j * BN;
+                if (block_needs_mask(p, q0, kv0)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int kj = kv0 + c * 32 + e;
+                            const bool vis = (kj < p.N) && (!p.causal || kj <= qi) &&
+                                             (p.window == 0 || qi - kj < p.window);
+                            if (!vis) sr[c][e] = __float_as_uint(-INFINITY);
+                        }
+                    }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    mx0 = fmaxf(mx0, __uint_as_float(sr[0][e]));
+                    mx1 = fmaxf(mx1, __uint_as_float(sr[1][e]));
+                    mx2 = fmaxf(mx2, __uint_as_float(sr[2][e]));
+                    mx3 = fmaxf(mx3, __uint_as_float(sr[3][e]));
+                }
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                float m_new = m_run;
+                if (mx > m_run + RESCALE_THRESHOLD) m_new = mx;
+                const float alpha = (m_new == m_run) ? 1.f : ptx::ex2(m_run - m_new);
+                m_run = m_new;
+                const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+
+                // P = 2^(x - m), its row sum, and P as bf16 over the first half of S
+                float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -mref));
+                        const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -mref));
+                        rs0 += p0;
+                        rs1 += p1;
+                        pk[e] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st16(t_s + 16 * c, pk);
+                }
+                l_run = l_run * alpha + (rs0 + rs1);
+                // O <- alpha * O, only when some row of this warp raised its maximum;
+                // the first KV tile needs none (its PV product overwrites O). Done after P is
+                // written so that the S registers are free.
+                if (j > lo && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld32(t_o + 32 * c, r);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        ptx::tmem_st32(t_o + 32 * c, r);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_p);
+            }
+            if (!ok) break;
+            ok = wait_warp(bar_o, o_use & 1u, abort_flag, limit);
+            ++o_use;
+            if (!ok) break;
+            ptx::tc_fence_after();
+            // epilogue: O / l -> bf16, and the natural-log LSE
+            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            const size_t ridx = static_cast<size_t>(w.b * p.Hq + w.hq) * static_cast<size_t>(p.N) +
+                                static_cast<size_t>(qi);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld32(t_o + 32 * c, r);
+                ptx::tmem_wait_ld();
+                if (qi < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D + 32 * c);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 val;
+                        val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 0]) * inv_l,
+                                                 __uint_as_float(r[8 * g + 1]) * inv_l);
+                        val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 2]) * inv_l,
+                                                 __uint_as_float(r[8 * g + 3]) * inv_l);
+                        val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 4]) * inv_l,
+                                                 __uint_as_float(r[8 * g + 5]) * inv_l);
+                        val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 6]) * inv_l,
+                                                 __uint_as_float(r[8 * g + 7]) * inv_l);
+                        dst[g] = val;
+                    }
+                }
+            }
+            if (qi < p.N) p.lse[ridx] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// One warp waits on a barrier nothing will complete; exercises the timeout path.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    wait_warp(ptx::smem_addr(&bar), 0u, &abort_flag, limit_ns);
+}
+
+}  // namespace attn
+
+// ====================================================================== host side
+namespace {
+
+using attn::Cfg;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready;
+    int sms;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return ATTN_ERR_CUDA;
+}
+
+EncodeTiledFn get_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// per-device one-time set-up: architecture check, SM count, shared-memory opt-in
+int device_setup(int *sms_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (!di.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+        // the warpgroup register split must fit in what a CTA is launched with;
+        // otherwise setmaxnreg.inc would wait for registers that never come
+        const void *kernels[2] = {reinterpret_cast<const void *>(attn::attn_fwd_kernel<64>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128>)};
+        for (const void *kfn : kernels) {
+            cudaFuncAttributes fa;
+            if ((e = cudaFuncGetAttributes(&fa, kfn)) != cudaSuccess) return cuda_fail(e);
+            if (fa.numRegs * attn::NUM_THREADS <
+                2 * 128 * attn::SOFTMAX_REGS + 128 * attn::PRODUCER_REGS)
+                return ATTN_ERR_UNSUPPORTED;
+        }
+        if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<128>::SMEM_ALLOC)) != cudaSuccess)
+            return cuda_fail(e);
+        di.sms = sms;
+        di.ready = true;
+    }
+    *sms_out = di.sms;
+    return ATTN_OK;
+}
+
+bool misaligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) != 0; }
+
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int B,
+             int Hq, int Hkv, int N, int d, int causal, int window, float scale) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULLPTR;
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || window < 0) return ATTN_ERR_SHAPE;
+    if (Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (causal != 0 && causal != 1) return ATTN_ERR_SHAPE;
+    if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;
+    // index range: rows fit 32-bit tile arithmetic; unit count fits int
+    if (N > (1 << 30)) return ATTN_ERR_SHAPE;
+    const long long bh = static_cast<long long>(B) * Hq;
+    const long long n_pairs = ((N + attn::BM - 1) / attn::BM + 1) / 2;
+    if (bh > INT_MAX || bh * n_pairs > INT_MAX) return ATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hkv > INT_MAX) return ATTN_ERR_SHAPE;
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+        misaligned(lse, 4))
+        return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
+int encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int N, long long BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
+    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(attn::BM), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return ATTN_OK;
+}
+
+template <int D>
+int launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+           int N, int causal, int window, float scale, cudaStream_t stream, int sms) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    CUtensorMap mq, mk, mv;
+    int rc;
+    if ((rc = encode_map(enc, &mq, q, D, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mk, k, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mv, v, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
+    attn::Params p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.N = N;
+    p.group = Hq / Hkv;
+    p.causal = causal;
+    p.window = window;
+    p.n_kv = (N + attn::BN - 1) / attn::BN;
+    p.n_pairs = (p.n_kv + 1) / 2;
+    p.num_units = B * Hq * p.n_pairs;
+    p.sl2 = scale * 1.4426950408889634f;
+    p.timeout_ns = attn::WAIT_LIMIT_NS;
+    const int grid = p.num_units < sms ? p.num_units : sms;
+    attn::attn_fwd_kernel<D><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+             int N, int d, int causal, int window, float scale, void *stream) {
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    int sms = 0;
+    if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 64) return launch<64>(q, k, v, o, lse, B, Hq, Hkv, N, causal, window, scale, s, sms);
+    return launch<128>(q, k, v, o, lse, B, Hq, Hkv, N, causal, window, scale, s, sms);
+}
+
+int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse, void *dq,
+                  void *dk, void *dv, void *do_, float *dlse, int B, int Hq, int Hkv, int N, int d,
+                  int causal, int window, float scale, void *stream) {
+    int rc = validate(dq, dk, dv, do_, dlse, B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    rc = validate(hq, hk, hv, ho, hlse, B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t q_bytes = static_cast<size_t>(B) * Hq * N * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(B) * Hkv * N * d * 2;
+    const size_t lse_bytes = static_cast<size_t>(B) * Hq * N * sizeof(float);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(dq, hq, q_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk, hk, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv, hv, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_fail(e);
+    rc = attn_fwd(dq, dk, dv, do_, dlse, B, Hq, Hkv, N, d, causal, window, scale, stream);
+    if (rc != ATTN_OK) return rc;
+    if ((e = cudaMemcpyAsync(ho, do_, q_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(hlse, dlse, lse_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e);
+    return ATTN_OK;
+}
+
+const char *attn_status_str(int status) {
+    switch (status) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_NULLPTR: return "ATTN_ERR_NULLPTR: a required pointer is NULL";
+        case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a buffer is not suitably aligned";
+        case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: invalid sizes, window or scale";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: head dim, mask or device not supported";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA runtime call failed";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait ran out of time";
+        default: return "unknown attn_status";
+    }
+}
+
+int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_device_error(int clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int word = 0;
+    if ((e = cudaMemcpyFromSymbol(&word, attn::g_status, sizeof word)) != cudaSuccess) return cuda_fail(e);
+    if (clear) {
+        const unsigned int zero = 0;
+        if ((e = cudaMemcpyToSymbol(attn::g_status, &zero, sizeof zero)) != cudaSuccess) return cuda_fail(e);
+    }
+    return (word & attn::STATUS_TIMEOUT) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(int64_t limit_ns) {
+    if (limit_ns < 1 || limit_ns > 1000000000LL) return ATTN_ERR_SHAPE;
+    int sms = 0;
+    int rc = device_setup(&sms);
+    if (rc != ATTN_OK) return rc;
+    attn::selftest_wait_kernel<<<1, 32>>>(static_cast<unsigned long long>(limit_ns));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return attn_device_error(1);
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

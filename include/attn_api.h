@@ -1,0 +1,134 @@
+/*
+ * attn_api.h -- C ABI of the B300 (sm_103a) exact self-attention forward library
+ * (libattn_fwd.so).
+ *
+ * The operation (every entry point below computes exactly this, up to rounding):
+ *
+ *   for every batch b, query head hq, query row i:
+ *     kv    = hq / (Hq / Hkv)                               grouped-query head map
+ *     J(i)  = { j : (!causal || j <= i) && (window == 0 || i - j < window) }
+ *     s_ij  = scale * q[b,hq,i,:] . k[b,kv,j,:]              for j in J(i)
+ *     lse_i = ln( sum_{j in J(i)} exp(s_ij) )                natural log, scale included
+ *     o[b,hq,i,:] = sum_{j in J(i)} exp(s_ij - lse_i) * v[b,kv,j,:]
+ *
+ * Sources, by page and section: the attention score QK^T/sqrt(D) and
+ * Attention = Softmax(score) V ("Background - Attention Mechanism" on the SpAtten
+ * review, coolstone2000.github.io); scaling by sqrt(d_k), the row softmax, the
+ * weighted sum of V, independent heads and the look-ahead mask under which a token
+ * attends to itself and earlier tokens (palettepath-it.com self-attention guide,
+ * sections on scaled dot-product scores, softmax normalisation, parallel heads and
+ * look-ahead masking); grouped-query and sliding-window attention as compared
+ * variants ("Attentions Under the Microscope" summary, gist.science, section
+ * "방법론"); the tensor layout [batch, heads, n, d] of the framework call
+ * F.scaled_dot_product_attention(q, k, v) (devhandbook.co.kr, Example 2). The head
+ * map kv = hq / G and the window rule i - j < window are readings of the pages,
+ * which name both variants without fixing either.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense and contiguous, row-major, in the layouts stated per
+ *     argument. bf16 means IEEE bfloat16 bit patterns (2 bytes).
+ *   - The caller owns every buffer. The library allocates nothing per call and keeps
+ *     only a per-device table of cached device attributes plus one device-side
+ *     status word per device (see attn_device_error).
+ *   - Calls are asynchronous with respect to the host on `stream` (a cudaStream_t
+ *     passed as void*; NULL = the legacy default stream) and never synchronise,
+ *     except attn_device_error and attn_selftest_wait_timeout, which say so.
+ *   - Argument errors are detected on the host before anything is launched or any
+ *     memory is touched; the call then returns a negative attn_status and has no
+ *     other effect. No error is fatal.
+ *   - Calls on different streams, from different host threads, are safe.
+ */
+#ifndef ATTN_API_H
+#define ATTN_API_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULLPTR = -1,     /* a required pointer is NULL */
+    ATTN_ERR_ALIGN = -2,       /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
+    ATTN_ERR_SHAPE = -3,       /* B, Hq, Hkv or N < 1; Hq % Hkv != 0; window < 0;
+                                  scale not finite and > 0; sizes beyond the index range */
+    ATTN_ERR_UNSUPPORTED = -4, /* d not 64 or 128; window > 0 without causal; the current
+                                  device is not an sm_103 (B300-class) GPU */
+    ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed; see attn_last_cuda_error */
+    ATTN_ERR_TIMEOUT = -6      /* a kernel wait gave up (reported by attn_device_error) */
+} attn_status;
+
+/*
+ * attn_fwd -- exact attention forward on device buffers.
+ *
+ *   q    device, bf16 [B, Hq,  N, d], 16-byte aligned (read)
+ *   k    device, bf16 [B, Hkv, N, d], 16-byte aligned (read)
+ *   v    device, bf16 [B, Hkv, N, d], 16-byte aligned (read)
+ *   o    device, bf16 [B, Hq,  N, d], 16-byte aligned (written; fp32 accumulation,
+ *        rounded to nearest even once at the end)
+ *   lse  device, fp32 [B, Hq, N], 4-byte aligned (written; natural-log log-sum-exp
+ *        of the scaled scores over J(i))
+ *   B, Hq, Hkv, N, d   sizes; Hq must be a multiple of Hkv; d is 64 or 128
+ *   causal  0 = bidirectional, 1 = look-ahead mask (j <= i)
+ *   window  0 = none; W > 0 (requires causal = 1) restricts keys to i-W+1 .. i
+ *   scale   multiplier of q.k (callers pass 1/sqrt(d)); finite and > 0
+ *   stream  cudaStream_t as void*
+ *
+ * o and lse must not overlap q, k or v. Returns ATTN_OK once the kernel is queued.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale,
+             void *stream);
+
+/*
+ * attn_fwd_host -- the same operation for callers whose tensors live in host memory.
+ *
+ * Queues on `stream`: one host-to-device copy each of q, k and v into the
+ * caller-owned device buffers dq, dk, dv; the attn_fwd kernel writing do_ and dlse;
+ * one device-to-host copy each of do_ and dlse into ho and hlse. Layouts, sizes and
+ * alignment rules are those of attn_fwd, for both the host and the device buffers.
+ * Host buffers should be page-locked (cudaHostAlloc / pinned) for the copies to be
+ * asynchronous; with pageable memory CUDA stages them synchronously. The results
+ * in ho and hlse are valid once `stream` has been synchronised. Nothing is
+ * allocated.
+ */
+int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse,
+                  void *dq, void *dk, void *dv, void *do_, float *dlse,
+                  int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale,
+                  void *stream);
+
+/* Human-readable name of an attn_status value (a static string; never NULL). */
+const char *attn_status_str(int status);
+
+/* cudaError_t of the most recent ATTN_ERR_CUDA returned on the calling host thread
+ * (0 if none). */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_device_error -- synchronises the current device, then reports whether any
+ * kernel of this library on it has given up a wait since the last clear: every
+ * pipeline wait inside the kernels is bounded (2 s); a wait that runs out sets a
+ * device-side status word, makes the kernel drain its own copies in flight, free
+ * its tensor memory and return. Returns ATTN_OK, ATTN_ERR_TIMEOUT, or
+ * ATTN_ERR_CUDA. clear != 0 resets the word after reading it.
+ */
+int attn_device_error(int clear);
+
+/*
+ * attn_selftest_wait_timeout -- exercises the bounded-wait failure path without a
+ * fault: launches one block that waits on a pipeline barrier that nothing will ever
+ * complete, with a limit of limit_ns nanoseconds (1 .. 10^9), synchronises, and
+ * returns what attn_device_error reports afterwards (expected: ATTN_ERR_TIMEOUT),
+ * clearing the status word. ATTN_ERR_SHAPE for a limit outside the range.
+ */
+int attn_selftest_wait_timeout(int64_t limit_ns);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_API_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import subprocess
+
+import pytest
+
+import exact_self_attention_fwd_b300 as ea
+from exact_self_attention_fwd_b300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_self_attention_fwd_b300 import build
+    build.build()
+    return ea.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = ea.header_functions()
+    assert set(names) >= {"attn_fwd", "attn_fwd_host", "attn_status_str", "attn_last_cuda_error",
+                          "attn_device_error", "attn_selftest_wait_timeout", "attn_version"}
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in names:
+        assert n in exported, f"{n} declared in attn_api.h but not exported"
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        s = lib.attn_status_str(code).decode()
+        assert s.startswith("ATTN_")
+    assert lib.attn_status_str(-99).decode() == "unknown attn_status"
+    assert lib.attn_version() >= 100
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device address": never dereferenced by these calls
+
+
+def call(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=1, Hkv=1, N=128, d=64, causal=0, window=0,
+         scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), ea.ATTN_ERR_NULLPTR),
+    (dict(lse=None), ea.ATTN_ERR_NULLPTR),
+    (dict(B=0), ea.ATTN_ERR_SHAPE),
+    (dict(N=0), ea.ATTN_ERR_SHAPE),
+    (dict(Hq=3, Hkv=2), ea.ATTN_ERR_SHAPE),
+    (dict(window=-1, causal=1), ea.ATTN_ERR_SHAPE),
+    (dict(scale=0.0), ea.ATTN_ERR_SHAPE),
+    (dict(scale=float("inf")), ea.ATTN_ERR_SHAPE),
+    (dict(scale=float("nan")), ea.ATTN_ERR_SHAPE),
+    (dict(causal=2), ea.ATTN_ERR_SHAPE),
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(window=16, causal=0), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(q=A + 8), ea.ATTN_ERR_ALIGN),
+    (dict(o=A + 2), ea.ATTN_ERR_ALIGN),
+    (dict(lse=A + 2), ea.ATTN_ERR_ALIGN),
+    (dict(N=(1 << 30) + 1), ea.ATTN_ERR_SHAPE),
+    (dict(B=1 << 16, Hq=1 << 16, Hkv=1 << 16), ea.ATTN_ERR_SHAPE),
+])
+def test_rejects_bad_arguments_before_launch(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_host_entry_validates_both_buffer_sets(lib):
+    args = [A] * 10 + [1, 1, 1, 128, 64, 0, 0, 0.125, None]
+    bad = list(args)
+    bad[0] = None
+    assert lib.attn_fwd_host(*bad) == ea.ATTN_ERR_NULLPTR
+    bad = list(args)
+    bad[9] = A + 1
+    assert lib.attn_fwd_host(*bad) == ea.ATTN_ERR_ALIGN
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.attn_selftest_wait_timeout(0) == ea.ATTN_ERR_SHAPE
+    assert lib.attn_selftest_wait_timeout(2_000_000_000) == ea.ATTN_ERR_SHAPE
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert call(lib) == ea.ATTN_ERR_CUDA
+    assert lib.attn_last_cuda_error() != 0
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ea.attn_fwd(q, q, q)

@@ -1,0 +1,183 @@
+"""The CUDA path (through the C ABI) against the fp64 oracle, element by element."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_self_attention_fwd_b300 as ea
+from exact_self_attention_fwd_b300.inputs import WORKLOADS, make_qkv, make_workload
+from parity import compare, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def run_gpu(q, k, v, causal, window, scale):
+    out, lse = ea.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.device_error() == ea.ATTN_OK
+    return out, lse
+
+
+def check_full(B, Hq, Hkv, N, d, causal, window, seed, scale=None, q_head0_scale=1.0):
+    q, k, v = make_qkv(B, Hq, Hkv, N, d, seed, q_head0_scale)
+    scale = scale or 1.0 / math.sqrt(d)
+    out, lse = run_gpu(q, k, v, causal, window, scale)
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, causal=causal, window=window, scale=scale)
+    return compare(out, lse, o_ref, lse_ref, f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} c{causal} W{window}")
+
+
+# ------------------------------------------------------------ sequence lengths and tails
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 2, 17, 127, 128, 129, 197, 255, 256, 257, 300, 513])
+def test_lengths(N, d, causal):
+    check_full(2, 3, 3, N, d, causal, 0, seed=1000 + N + d + int(causal))
+
+
+# ------------------------------------------------------------ grouped-query heads
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa(G, causal):
+    check_full(2, 8, 8 // G, 300, 128, causal, 0, seed=2000 + G)
+    check_full(1, 8, 8 // G, 260, 64, causal, 0, seed=2100 + G)
+
+
+# ------------------------------------------------------------ sliding window
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("W", [1, 2, 100, 127, 128, 129, 255, 256, 300, 599, 600, 1000])
+def test_window(W, d):
+    check_full(1, 2, 1, 600, d, True, W, seed=3000 + W)
+
+
+def test_window_ge_n_equals_causal():
+    q, k, v = make_qkv(1, 4, 2, 333, 128, 77)
+    a = run_gpu(q, k, v, True, 0, 0.088)
+    b = run_gpu(q, k, v, True, 333, 0.088)
+    c = run_gpu(q, k, v, True, 5000, 0.088)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[0], c[0])
+    assert torch.equal(a[1], b[1]) and torch.equal(a[1], c[1])
+
+
+# ------------------------------------------------------------ softmax range
+@pytest.mark.parametrize("mult", [0.0, 4.0, 16.0])
+def test_sharp_and_flat_softmax(mult):
+    g = torch.Generator().manual_seed(5)
+    q = (mult * torch.randn(1, 2, 384, 64, generator=g)).bfloat16()
+    k = torch.randn(1, 2, 384, 64, generator=g).bfloat16()
+    v = torch.randn(1, 2, 384, 64, generator=g).bfloat16()
+    for causal in (False, True):
+        out, lse = run_gpu(q, k, v, causal, 0, 0.125)
+        o_ref, lse_ref = oracle.attn_ref(q, k, v, causal=causal, scale=0.125)
+        compare(out, lse, o_ref, lse_ref, f"mult {mult} causal {causal}")
+
+
+def test_many_units_per_cta():
+    # more work units than SMs: exercises the persistent loop and barrier phases
+    check_full(4, 40, 8, 520, 64, True, 0, seed=6)
+    check_full(3, 64, 16, 260, 128, False, 0, seed=7)
+
+
+# ------------------------------------------------------------ the five workloads
+def test_workload_tiny():
+    w = WORKLOADS["tiny"]
+    q, k, v = make_workload(w)
+    out, lse = run_gpu(q, k, v, w.causal, w.window, w.scale)
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, causal=w.causal, window=w.window, scale=w.scale)
+    compare(out, lse, o_ref, lse_ref, w.name)
+
+
+@pytest.mark.parametrize("name", ["vit_base", "gpt2_small"])
+def test_workload_full(name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    out, lse = run_gpu(q, k, v, w.causal, w.window, w.scale)
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, causal=w.causal, window=w.window, scale=w.scale)
+    stats = compare(out, lse, o_ref, lse_ref, w.name)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["gqa_8k", "swa_16k"])
+def test_workload_sampled(name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    out, lse = run_gpu(q, k, v, w.causal, w.window, w.scale)
+    rows = sample_rows(w.B, w.Hq, w.N, w.window, n_random=600, seed=w.seed)
+    o_ref, lse_ref = oracle.attn_ref_rows(q, k, v, w.causal, w.window, w.scale, rows)
+    stats = compare(out.reshape(-1, w.d)[torch.from_numpy(rows).to(DEV)],
+                    lse.reshape(-1)[torch.from_numpy(rows).to(DEV)], o_ref, lse_ref, w.name)
+    print(name, len(rows), stats)
+    # properties of every row at full size: finite, a convex combination of V rows, and
+    # lse_i >= s_ii (the diagonal is always visible)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    vmax = v.float().abs().amax().item()
+    assert out.float().abs().amax().item() <= vmax * (1 + 2 ** -7)
+    G = w.group
+    qd = q.to(DEV).float()
+    kd = k.to(DEV).float().repeat_interleave(G, dim=1)
+    s_ii = (qd * kd).sum(-1) * w.scale
+    assert bool((lse >= s_ii - 1e-3 * s_ii.abs().clamp(min=1)).all())
+
+
+# ------------------------------------------------------------ determinism, streams, host entry
+def test_deterministic():
+    q, k, v = make_qkv(2, 8, 2, 1000, 128, 8)
+    a = run_gpu(q, k, v, True, 0, 0.09)
+    b = run_gpu(q, k, v, True, 0, 0.09)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_side_stream_matches_default():
+    q, k, v = make_qkv(1, 4, 4, 400, 64, 9)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    a = ea.attn_fwd(qd, kd, vd, causal=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        b = ea.attn_fwd(qd, kd, vd, causal=True, stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_host_entry_matches_device_entry():
+    B, Hq, Hkv, N, d = 2, 8, 4, 300, 128
+    q, k, v = make_qkv(B, Hq, Hkv, N, d, 10)
+    ref = run_gpu(q, k, v, True, 64, 0.1)
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty_like(q).pin_memory()
+    hl = torch.empty(B, Hq, N, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q, device=DEV), torch.empty_like(k, device=DEV), torch.empty_like(v, device=DEV)
+    do = torch.empty_like(q, device=DEV)
+    dl = torch.empty(B, Hq, N, dtype=torch.float32, device=DEV)
+    ea.attn_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, causal=True, window=64, scale=0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(ho, ref[0].cpu()) and torch.equal(hl, ref[1].cpu())
+
+
+def test_output_buffers_untouched_outside_shape():
+    # the kernel writes exactly B*Hq*N rows: a guard region after O and LSE stays intact
+    q, k, v = make_qkv(1, 2, 2, 197, 64, 11)
+    big_o = torch.full((2 * 197 * 64 + 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    big_l = torch.full((2 * 197 + 1024,), 7.0, dtype=torch.float32, device=DEV)
+    o = big_o[: 2 * 197 * 64].view(1, 2, 197, 64)
+    l = big_l[: 2 * 197].view(1, 2, 197)
+    ea.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), out=o, lse=l)
+    torch.cuda.synchronize()
+    assert bool((big_o[2 * 197 * 64:] == 7.0).all()) and bool((big_l[2 * 197:] == 7.0).all())
+
+
+def test_bad_arguments_raise():
+    q = torch.zeros(1, 3, 64, 64, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ea.AttnError) as e:
+        ea.attn_fwd(q, k, k)
+    assert e.value.code == ea.ATTN_ERR_SHAPE
+    q = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ea.AttnError) as e:
+        ea.attn_fwd(q, q, q)
+    assert e.value.code == ea.ATTN_ERR_UNSUPPORTED
