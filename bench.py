@@ -368,7 +368,7 @@ def run_ours(args, w: Workload):
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     local_total = sum(per) / 1e3
     total = max_over_ranks(dist, local_total)
-    value = F * world / total / 1e12
+    value = F * world * args.steps / total / 1e12
     ms_step = 1e3 * total / args.steps
     srt = sorted(per)
     cut = int(len(srt) * 0.15)

@@ -501,7 +501,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 m_run = m_new;
                 const float mref = (m_run == -INFINITY) ? 0.f : m_run;
 
-                // P = 2^(x - m), its row sum, and P as bf16 over the first half of S
+                // P = 2^(x - m) as bf16 over the first half of S, and the row sum of the
+                // ROUNDED P: O is then normalised by exactly the weights the tensor core
+                // used, a true convex combination of V rows, so the rounding of a
+                // dominant weight cancels instead of showing up in O.
                 float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -510,9 +513,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int e = 0; e < 16; ++e) {
                         const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -mref));
                         const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -mref));
-                        rs0 += p0;
-                        rs1 += p1;
                         pk[e] = ptx::pack_bf16x2(p0, p1);
+                        rs0 += __uint_as_float(pk[e] << 16);
+                        rs1 += __uint_as_float(pk[e] & 0xFFFF0000u);
                     }
                     ptx::tmem_st16(t_s + 16 * c, pk);
                 }
