@@ -64,6 +64,7 @@ constexpr uint32_t STATUS_TIMEOUT = 1u;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr float LN2 = 0.693147180559945309f;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr uint32_t WAIT_SLEEP_NS = 200000u;  // a waiting thread re-checks at least this often
 
 __device__ unsigned int g_status;  // bit 0: some wait ran out of time
 
@@ -92,8 +93,8 @@ struct Cfg {
     static constexpr int B_KVFULL = 3;              // STAGES
     static constexpr int B_KVEMPTY = 3 + STAGES;    // STAGES
     static constexpr int B_SFULL = 3 + 2 * STAGES;  // 2
-    static constexpr int B_PFULL = B_SFULL + 2;     // 2
-    static constexpr int B_OFULL = B_PFULL + 2;     // 2
+    static constexpr int B_PFULL = B_SFULL + 2;     // 4: (tile, half of P)
+    static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_DRAIN = B_OFULL + 2;     // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
@@ -121,7 +122,7 @@ __device__ bool wait_one(uint32_t bar, uint32_t parity, volatile uint32_t *abort
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
         if (*abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > limit) {
             raise_timeout(abort_flag);
@@ -136,7 +137,7 @@ __device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abor
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     while (true) {
-        const bool ok = ptx::mbar_try_wait(bar, parity);
+        const bool ok = ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS);
         if (__all_sync(0xffffffffu, ok)) return true;
         int give_up = 0;
         if (lane == 0) {
@@ -233,7 +234,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(C::B_SFULL + t), 1);
-            ptx::mbar_init(bar(C::B_PFULL + t), 4);  // one arrival per softmax warp
+            ptx::mbar_init(bar(C::B_PFULL + 2 * t + 0), 4);  // one arrival per softmax warp
+            ptx::mbar_init(bar(C::B_PFULL + 2 * t + 1), 4);
             ptx::mbar_init(bar(C::B_OFULL + t), 1);
         }
         ptx::mbar_init(bar(C::B_DRAIN), 1);
@@ -341,15 +343,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::mma_ss(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
                     }
                 };
-                // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory
-                auto issue_pv = [&](uint32_t col_o, uint32_t col_s, uint32_t vslot, bool accumulate) {
+                // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory.
+                // The softmax warps hand P over in two halves of 64 keys each; the MMAs of
+                // the first half are issued as soon as it is written, while the second half
+                // is still being computed.
+                auto issue_pv = [&](int t, uint32_t col_o, uint32_t col_s, uint32_t vslot,
+                                    bool accumulate, uint32_t parity) -> bool {
                     const uint64_t vd = ptx::sdesc_sw128(sb + C::SMEM_KV + vslot * C::TILE_BYTES,
                                                          C::CHUNK_BYTES, 1024);
     #pragma unroll 1
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        ptx::mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4), IDESC_PV,
-                                    (accumulate || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait_one(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
+                        ptx::tc_fence_after();
+    #pragma unroll 1
+                        for (int kk = h * (BN / 32); kk < (h + 1) * (BN / 32); ++kk) {
+                            ptx::mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4),
+                                        IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+                        }
                     }
+                    return true;
                 };
                 const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
 
@@ -383,11 +395,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tc_fence_after();
                         // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
                         if (prev >= lo0 && prev < hi0) {
-                            ok = wait_one(bar(C::B_PFULL + 0), p_use0 & 1u, abort_flag, limit);
+                            ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
                             ++p_use0;
                             if (!ok) break;
-                            ptx::tc_fence_after();
-                            issue_pv(C::COL_O0, C::COL_S0, vprev, prev > lo0);
                         }
                         if (j >= lo0 && j < hi0) {
                             issue_s(qa0, C::COL_S0, ks);
@@ -395,11 +405,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         // tile 1: the same, overlapping softmax of tile 0
                         if (has1 && prev >= lo1 && prev < hi1) {
-                            ok = wait_one(bar(C::B_PFULL + 1), p_use1 & 1u, abort_flag, limit);
+                            ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
                             ++p_use1;
                             if (!ok) break;
-                            ptx::tc_fence_after();
-                            issue_pv(C::COL_O1, C::COL_S1, vprev, prev > lo1);
                         }
                         if (has1 && j >= lo1 && j < hi1) {
                             issue_s(qa1, C::COL_S1, ks);
@@ -417,20 +425,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!ok) break;
                     ptx::tc_fence_after();
                     if (prev >= lo0 && prev < hi0) {
-                        ok = wait_one(bar(C::B_PFULL + 0), p_use0 & 1u, abort_flag, limit);
+                        ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
                         ++p_use0;
                         if (!ok) break;
-                        ptx::tc_fence_after();
-                        issue_pv(C::COL_O0, C::COL_S0, vprev, prev > lo0);
                     }
                     ptx::mma_commit(bar(C::B_OFULL + 0));
                     if (has1) {
                         if (prev >= lo1 && prev < hi1) {
-                            ok = wait_one(bar(C::B_PFULL + 1), p_use1 & 1u, abort_flag, limit);
+                            ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
                             ++p_use1;
                             if (!ok) break;
-                            ptx::tc_fence_after();
-                            issue_pv(C::COL_O1, C::COL_S1, vprev, prev > lo1);
                         }
                         ptx::mma_commit(bar(C::B_OFULL + 1));
                     }
@@ -451,7 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
-        const uint32_t bar_s = bar(C::B_SFULL + t), bar_p = bar(C::B_PFULL + t), bar_o = bar(C::B_OFULL + t);
+        const uint32_t bar_s = bar(C::B_SFULL + t), bar_o = bar(C::B_OFULL + t);
+        const uint32_t bar_p0 = bar(C::B_PFULL + 2 * t), bar_p1 = bar(C::B_PFULL + 2 * t + 1);
         const float sl2 = p.sl2;
         uint32_t s_use = 0, o_use = 0;
         bool ok = true;
@@ -463,7 +468,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (hi <= lo) continue;
             const int qi = q0 + row;
             float m_run = -INFINITY;  // running max of scale*s*log2(e)
-            float l_run = 0.f;        // running sum of 2^(x - m_run)
+            float l_run = 0.f;        // running sum of 2^(x - m_run), for the LSE
+            float r_run = 0.f;        // running sum of bf16(2^(x - m_run)), for normalising O
             for (int j = lo; j < hi; ++j) {
                 ok = wait_warp(bar_s, s_use & 1u, abort_flag, limit);
                 ++s_use;
@@ -486,45 +492,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                // row maximum: four independent chains of three-input max
+                float mxc[4];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sr[0][e]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sr[1][e]));
-                    mx2 = fmaxf(mx2, __uint_as_float(sr[2][e]));
-                    mx3 = fmaxf(mx3, __uint_as_float(sr[3][e]));
+                for (int c = 0; c < 4; ++c) {
+                    float a = __uint_as_float(sr[c][0]);
+#pragma unroll
+                    for (int e = 1; e < 31; e += 2)
+                        a = ptx::fmax3(a, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                    mxc[c] = fmaxf(a, __uint_as_float(sr[c][31]));
                 }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const float mx = ptx::fmax3(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * sl2;
                 float m_new = m_run;
                 if (mx > m_run + RESCALE_THRESHOLD) m_new = mx;
                 const float alpha = (m_new == m_run) ? 1.f : ptx::ex2(m_run - m_new);
                 m_run = m_new;
                 const float mref = (m_run == -INFINITY) ? 0.f : m_run;
 
-                // P = 2^(x - m) as bf16 over the first half of S, and the row sum of the
-                // ROUNDED P: O is then normalised by exactly the weights the tensor core
-                // used, a true convex combination of V rows, so the rounding of a
-                // dominant weight cancels instead of showing up in O.
-                float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -mref));
-                        const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -mref));
-                        pk[e] = ptx::pack_bf16x2(p0, p1);
-                        rs0 += __uint_as_float(pk[e] << 16);
-                        rs1 += __uint_as_float(pk[e] & 0xFFFF0000u);
-                    }
-                    ptx::tmem_st16(t_s + 16 * c, pk);
-                }
-                l_run = l_run * alpha + (rs0 + rs1);
-                // O <- alpha * O, only when some row of this warp raised its maximum;
-                // the first KV tile needs none (its PV product overwrites O). Done after P is
-                // written so that the S registers are free.
+                // O <- alpha * O, only when some row of this warp raised its maximum; the
+                // first KV tile needs none (its PV product overwrites O). The previous PV
+                // product has completed: the S commit this warp waited for follows it.
                 if (j > lo && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
                         ptx::tmem_ld32(t_o + 32 * c, r);
@@ -534,18 +523,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tmem_st32(t_o + 32 * c, r);
                     }
                 }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_p);
+
+                // P = 2^(x - m) as bf16 over the first half of S, handed to the MMA warp in
+                // two halves of 64 keys. Two row sums: the exact one (for the LSE) and the
+                // sum of the ROUNDED P, by which O is normalised: O is then an exact convex
+                // combination of V rows under the weights the tensor core actually used,
+                // so the rounding of a dominant weight cancels instead of showing in O.
+                const float2 sl2x2 = make_float2(sl2, sl2);
+                const float2 negm = make_float2(-mref, -mref);
+                float2 le0 = make_float2(0.f, 0.f), le1 = make_float2(0.f, 0.f);
+                float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int c = 2 * h; c < 2 * h + 2; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = make_float2(__uint_as_float(sr[c][2 * e]),
+                                                         __uint_as_float(sr[c][2 * e + 1]));
+                            const float2 a = __ffma2_rn(x, sl2x2, negm);
+                            const float2 pe = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                            pk[e] = ptx::pack_bf16x2(pe.x, pe.y);
+                            if (e & 1) {
+                                le1 = __fadd2_rn(le1, pe);
+                                ptx::add_bf16x2_halves(lr2, lr3, pk[e]);
+                            } else {
+                                le0 = __fadd2_rn(le0, pe);
+                                ptx::add_bf16x2_halves(lr0, lr1, pk[e]);
+                            }
+                        }
+                        ptx::tmem_st16(t_s + 16 * c, pk);
+                    }
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(h ? bar_p1 : bar_p0);
+                }
+                l_run = l_run * alpha + ((le0.x + le0.y) + (le1.x + le1.y));
+                r_run = r_run * alpha + ((lr0 + lr1) + (lr2 + lr3));
             }
             if (!ok) break;
             ok = wait_warp(bar_o, o_use & 1u, abort_flag, limit);
             ++o_use;
             if (!ok) break;
             ptx::tc_fence_after();
-            // epilogue: O / l -> bf16, and the natural-log LSE
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            // epilogue: O / (sum of rounded P) -> bf16, and the natural-log LSE
+            const float inv_l = r_run > 0.f ? 1.f / r_run : 0.f;
             const size_t ridx = static_cast<size_t>(w.b * p.Hq + w.hq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
 #pragma unroll
