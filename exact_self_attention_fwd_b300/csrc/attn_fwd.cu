@@ -10,8 +10,10 @@
 //   warps 4-7   softmax warpgroup for query tile 1
 //   warp 8      TMA producer: Q tiles once per unit, then K_j, V_j through a ring of
 //               shared-memory stages guarded by full/empty mbarriers
-//   warp 9      tensor-memory owner and MMA issuer (one thread): S_t = Q_t K_j^T into
-//               tensor memory, then O_t += P_t V_j with P_t read from tensor memory
+//   warp 9      tensor-memory owner and MMA issuer: S_t = Q_t K_j^T into tensor memory,
+//               then O_t += P_t V_j with P_t read from tensor memory
+//   (warps 8 and 9 run their loops on all lanes with warp-uniform values and issue
+//   each copy, MMA and commit from one lane elected inside the instruction's asm)
 //   warps 10-11 idle; with warps 8-9 they form the warpgroup that hands registers to
 //               the softmax warpgroups (setmaxnreg)
 // A work unit is two consecutive 128-row query tiles of one (batch, query head); both
@@ -262,188 +264,187 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         if (warp == WARP_TMA) {
             // ============================================================ TMA producer
-            if (lane == 0) {
-                uint32_t kv_it = 0, q_it = 0, q_loads0 = 0, q_loads1 = 0;
-                bool ok = true;
-                for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                    const Unit w = decode_unit(u, p);
-                    const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
-                    int lo0, hi0, lo1, hi1;
-                    tile_range(p, q0a, lo0, hi0);
-                    tile_range(p, q0b, lo1, hi1);
-                    const bool has1 = hi1 > lo1;
-                    const int lo = has1 ? min(lo0, lo1) : lo0;
-                    const int hi = has1 ? max(hi0, hi1) : hi0;
-                    const int zq = w.b * p.Hq + w.hq;
-                    const int zkv = w.b * p.Hkv + w.hkv;
-                    ok = wait_one(bar(C::B_QEMPTY), (q_it & 1u) ^ 1u, abort_flag, limit);
-                    ++q_it;
-                    if (!ok) break;
-                    ptx::mbar_arrive_expect_tx(bar(C::B_QFULL + 0), C::TILE_BYTES);
-    #pragma unroll 1
+            // All 32 lanes run this loop with identical values; each copy is issued by one
+            // elected lane.
+            uint32_t kv_it = 0, q_it = 0, q_loads0 = 0, q_loads1 = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p);
+                const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
+                int lo0, hi0, lo1, hi1;
+                tile_range(p, q0a, lo0, hi0);
+                tile_range(p, q0b, lo1, hi1);
+                const bool has1 = hi1 > lo1;
+                const int lo = has1 ? min(lo0, lo1) : lo0;
+                const int hi = has1 ? max(hi0, hi1) : hi0;
+                const int zq = w.b * p.Hq + w.hq;
+                const int zkv = w.b * p.Hkv + w.hkv;
+                ok = wait_warp(bar(C::B_QEMPTY), (q_it & 1u) ^ 1u, abort_flag, limit);
+                ++q_it;
+                if (!ok) break;
+                ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 0), C::TILE_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::NCHUNK; ++c)
+                    ptx::tma_load_3d_elect(sb + C::SMEM_Q + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 0),
+                                           c * 64, q0a, zq);
+                ++q_loads0;
+                if (has1) {
+                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 1), C::TILE_BYTES);
+#pragma unroll
                     for (int c = 0; c < C::NCHUNK; ++c)
-                        ptx::tma_load_3d(sb + C::SMEM_Q + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 0),
-                                         c * 64, q0a, zq);
-                    ++q_loads0;
-                    if (has1) {
-                        ptx::mbar_arrive_expect_tx(bar(C::B_QFULL + 1), C::TILE_BYTES);
-    #pragma unroll 1
-                        for (int c = 0; c < C::NCHUNK; ++c)
-                            ptx::tma_load_3d(sb + C::SMEM_Q + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
-                                             bar(C::B_QFULL + 1), c * 64, q0b, zq);
-                        ++q_loads1;
-                    }
-                    for (int j = lo; ok && j < hi; ++j) {
-    #pragma unroll 1
-                        for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
-                            const uint32_t s = kv_it % C::STAGES;
-                            const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
-                            if (ok) ok = wait_one(bar(C::B_KVEMPTY + s), ph, abort_flag, limit);
-                            if (ok) {
-                                ptx::mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE_BYTES);
-                                const CUtensorMap *m = kv ? &tm_v : &tm_k;
-    #pragma unroll 1
-                                for (int c = 0; c < C::NCHUNK; ++c)
-                                    ptx::tma_load_3d(sb + C::SMEM_KV + s * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                                     m, bar(C::B_KVFULL + s), c * 64, j * BN, zkv);
-                                ++kv_it;
-                            }
-                        }
-                    }
+                        ptx::tma_load_3d_elect(sb + C::SMEM_Q + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
+                                               bar(C::B_QFULL + 1), c * 64, q0b, zq);
+                    ++q_loads1;
                 }
-                if (!ok) {
-                    // let every copy this thread issued land before the CTA exits
-                    for (uint32_t s = 0; s < static_cast<uint32_t>(C::STAGES); ++s) {
-                        if (kv_it <= s) continue;
-                        const uint32_t last = (kv_it - 1u - s) / C::STAGES * C::STAGES + s;
-                        drain_wait(bar(C::B_KVFULL + s), (last / C::STAGES) & 1u, 100000000ull);
+                for (int j = lo; ok && j < hi; ++j) {
+#pragma unroll 1
+                    for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
+                        const uint32_t st = kv_it % C::STAGES;
+                        const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
+                        ok = wait_warp(bar(C::B_KVEMPTY + st), ph, abort_flag, limit);
+                        if (!ok) break;
+                        ptx::mbar_arrive_expect_tx_elect(bar(C::B_KVFULL + st), C::TILE_BYTES);
+                        const CUtensorMap *m = kv ? &tm_v : &tm_k;
+#pragma unroll
+                        for (int c = 0; c < C::NCHUNK; ++c)
+                            ptx::tma_load_3d_elect(sb + C::SMEM_KV + st * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                                   m, bar(C::B_KVFULL + st), c * 64, j * BN, zkv);
+                        ++kv_it;
                     }
-                    if (q_loads0) drain_wait(bar(C::B_QFULL + 0), (q_loads0 - 1u) & 1u, 100000000ull);
-                    if (q_loads1) drain_wait(bar(C::B_QFULL + 1), (q_loads1 - 1u) & 1u, 100000000ull);
                 }
             }
-            __syncwarp();
+            if (!ok) {
+                // let every copy this warp issued land before the CTA exits
+                for (uint32_t st = 0; st < static_cast<uint32_t>(C::STAGES); ++st) {
+                    if (kv_it <= st) continue;
+                    const uint32_t last = (kv_it - 1u - st) / C::STAGES * C::STAGES + st;
+                    drain_wait(bar(C::B_KVFULL + st), (last / C::STAGES) & 1u, 100000000ull);
+                }
+                if (q_loads0) drain_wait(bar(C::B_QFULL + 0), (q_loads0 - 1u) & 1u, 100000000ull);
+                if (q_loads1) drain_wait(bar(C::B_QFULL + 1), (q_loads1 - 1u) & 1u, 100000000ull);
+            }
         } else if (warp == WARP_MMA) {
             // ============================================================ MMA issuer
-            if (lane == 0) {
-                constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
-                constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
-                uint32_t kv_it = 0, q_use0 = 0, q_use1 = 0, p_use0 = 0, p_use1 = 0;
-                bool ok = true;
+            // All 32 lanes run this loop with identical values (so descriptors and tensor
+            // memory addresses are warp-uniform); each MMA and commit is issued by one
+            // elected lane.
+            constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
+            uint32_t kv_it = 0, q_use0 = 0, q_use1 = 0, p_use0 = 0, p_use1 = 0;
+            bool ok = true;
 
-                // S_t = Q_t K^T: K-major A and B, 16 columns of d per instruction. The
-                // descriptors of later K steps differ only in the start-address field, so
-                // they are formed by adding the byte offset >> 4 to the first one.
-                auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
-                    const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
-                    const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
-    #pragma unroll 1
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+            // S_t = Q_t K^T: K-major A and B, 16 columns of d per instruction. The
+            // descriptors of later K steps differ only in the start-address field, so
+            // they are formed by adding the byte offset >> 4 to the first one.
+            auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
+                const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
+                const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss_elect(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory.
+            // The softmax warps hand P over in two halves of 64 keys each; the MMAs of
+            // the first half are issued as soon as it is written, while the second half
+            // is still being computed.
+            auto issue_pv = [&](int t, uint32_t col_o, uint32_t col_s, uint32_t vslot,
+                                bool accumulate, uint32_t parity) -> bool {
+                const uint64_t vd = ptx::sdesc_sw128(sb + C::SMEM_KV + vslot * C::TILE_BYTES,
+                                                     C::CHUNK_BYTES, 1024);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    if (!wait_warp(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int kk = h * (BN / 32); kk < (h + 1) * (BN / 32); ++kk) {
+                        ptx::mma_ts_elect(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4),
+                                          IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
                     }
-                };
-                // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory.
-                // The softmax warps hand P over in two halves of 64 keys each; the MMAs of
-                // the first half are issued as soon as it is written, while the second half
-                // is still being computed.
-                auto issue_pv = [&](int t, uint32_t col_o, uint32_t col_s, uint32_t vslot,
-                                    bool accumulate, uint32_t parity) -> bool {
-                    const uint64_t vd = ptx::sdesc_sw128(sb + C::SMEM_KV + vslot * C::TILE_BYTES,
-                                                         C::CHUNK_BYTES, 1024);
-    #pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        if (!wait_one(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
-                        ptx::tc_fence_after();
-    #pragma unroll 1
-                        for (int kk = h * (BN / 32); kk < (h + 1) * (BN / 32); ++kk) {
-                            ptx::mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4),
-                                        IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
-                        }
-                    }
-                    return true;
-                };
-                const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
+                }
+                return true;
+            };
+            const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
 
-                for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                    const Unit w = decode_unit(u, p);
-                    const int q0a = 2 * w.pair * BM;
-                    int lo0, hi0, lo1, hi1;
-                    tile_range(p, q0a, lo0, hi0);
-                    tile_range(p, q0a + BM, lo1, hi1);
-                    const bool has1 = hi1 > lo1;
-                    const int lo = has1 ? min(lo0, lo1) : lo0;
-                    const int hi = has1 ? max(hi0, hi1) : hi0;
-                    ok = wait_one(bar(C::B_QFULL + 0), q_use0 & 1u, abort_flag, limit);
-                    ++q_use0;
-                    if (ok && has1) {
-                        ok = wait_one(bar(C::B_QFULL + 1), q_use1 & 1u, abort_flag, limit);
-                        ++q_use1;
-                    }
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p);
+                const int q0a = 2 * w.pair * BM;
+                int lo0, hi0, lo1, hi1;
+                tile_range(p, q0a, lo0, hi0);
+                tile_range(p, q0a + BM, lo1, hi1);
+                const bool has1 = hi1 > lo1;
+                const int lo = has1 ? min(lo0, lo1) : lo0;
+                const int hi = has1 ? max(hi0, hi1) : hi0;
+                ok = wait_warp(bar(C::B_QFULL + 0), q_use0 & 1u, abort_flag, limit);
+                ++q_use0;
+                if (ok && has1) {
+                    ok = wait_warp(bar(C::B_QFULL + 1), q_use1 & 1u, abort_flag, limit);
+                    ++q_use1;
+                }
+                if (!ok) break;
+                ptx::tc_fence_after();
+                int prev = -1;
+                uint32_t vprev = 0, vprev_ph = 0;
+                for (int j = lo; j < hi; ++j) {
+                    const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
+                    ++kv_it;
+                    const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
+                    ++kv_it;
+                    ok = wait_warp(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
+                    if (ok && prev >= 0) ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    int prev = -1;
-                    uint32_t vprev = 0, vprev_ph = 0;
-                    for (int j = lo; j < hi; ++j) {
-                        const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
-                        ++kv_it;
-                        const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
-                        ++kv_it;
-                        ok = wait_one(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
-                        if (ok && prev >= 0) ok = wait_one(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                        // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
-                        if (prev >= lo0 && prev < hi0) {
-                            ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
-                            ++p_use0;
-                            if (!ok) break;
-                        }
-                        if (j >= lo0 && j < hi0) {
-                            issue_s(qa0, C::COL_S0, ks);
-                            ptx::mma_commit(bar(C::B_SFULL + 0));
-                        }
-                        // tile 1: the same, overlapping softmax of tile 0
-                        if (has1 && prev >= lo1 && prev < hi1) {
-                            ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
-                            ++p_use1;
-                            if (!ok) break;
-                        }
-                        if (has1 && j >= lo1 && j < hi1) {
-                            issue_s(qa1, C::COL_S1, ks);
-                            ptx::mma_commit(bar(C::B_SFULL + 1));
-                        }
-                        if (prev >= 0) ptx::mma_commit(bar(C::B_KVEMPTY + vprev));
-                        ptx::mma_commit(bar(C::B_KVEMPTY + ks));
-                        prev = j;
-                        vprev = vs;
-                        vprev_ph = vph;
-                    }
-                    if (!ok) break;
-                    ptx::mma_commit(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
-                    ok = wait_one(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
+                    // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
                     if (prev >= lo0 && prev < hi0) {
                         ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
                         ++p_use0;
                         if (!ok) break;
                     }
-                    ptx::mma_commit(bar(C::B_OFULL + 0));
-                    if (has1) {
-                        if (prev >= lo1 && prev < hi1) {
-                            ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
-                            ++p_use1;
-                            if (!ok) break;
-                        }
-                        ptx::mma_commit(bar(C::B_OFULL + 1));
+                    if (j >= lo0 && j < hi0) {
+                        issue_s(qa0, C::COL_S0, ks);
+                        ptx::mma_commit_elect(bar(C::B_SFULL + 0));
                     }
-                    ptx::mma_commit(bar(C::B_KVEMPTY + vprev));
+                    // tile 1: the same, overlapping softmax of tile 0
+                    if (has1 && prev >= lo1 && prev < hi1) {
+                        ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
+                        ++p_use1;
+                        if (!ok) break;
+                    }
+                    if (has1 && j >= lo1 && j < hi1) {
+                        issue_s(qa1, C::COL_S1, ks);
+                        ptx::mma_commit_elect(bar(C::B_SFULL + 1));
+                    }
+                    if (prev >= 0) ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
+                    ptx::mma_commit_elect(bar(C::B_KVEMPTY + ks));
+                    prev = j;
+                    vprev = vs;
+                    vprev_ph = vph;
                 }
-                // every MMA this thread issued completes before tensor memory is freed
-                ptx::mma_commit(bar(C::B_DRAIN));
-                drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
+                if (!ok) break;
+                ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if (prev >= lo0 && prev < hi0) {
+                    ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
+                    ++p_use0;
+                    if (!ok) break;
+                }
+                ptx::mma_commit_elect(bar(C::B_OFULL + 0));
+                if (has1) {
+                    if (prev >= lo1 && prev < hi1) {
+                        ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
+                        ++p_use1;
+                        if (!ok) break;
+                    }
+                    ptx::mma_commit_elect(bar(C::B_OFULL + 1));
+                }
+                ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
             }
+            // every MMA this warp issued completes before tensor memory is freed
+            ptx::mma_commit_elect(bar(C::B_DRAIN));
+            drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
             __syncwarp();
         }
     } else {
