@@ -57,8 +57,8 @@ constexpr int NUM_THREADS = 384;  // 3 warpgroups; warps 10-11 only hold registe
 // warpgroup gives registers back and the two softmax warpgroups take them, so that
 // 2 * 128 * SOFTMAX_REGS + 128 * PRODUCER_REGS equals the launch total exactly.
 constexpr int LAUNCH_REGS = 168;
-constexpr int PRODUCER_REGS = 56;
-constexpr int SOFTMAX_REGS = 224;
+constexpr int PRODUCER_REGS = 72;
+constexpr int SOFTMAX_REGS = 216;
 static_assert(2 * 128 * SOFTMAX_REGS + 128 * PRODUCER_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch allocation");
 constexpr uint32_t TMEM_COLS = 512;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
                 const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
                 const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
                     ptx::mma_ss_elect(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
@@ -357,10 +357,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int h = 0; h < 2; ++h) {
                     if (!wait_warp(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
                     ptx::tc_fence_after();
-#pragma unroll 1
-                    for (int kk = h * (BN / 32); kk < (h + 1) * (BN / 32); ++kk) {
-                        ptx::mma_ts_elect(tmem + col_o, tmem + col_s + kk * 8, vd + ((kk * 2048) >> 4),
-                                          IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 32; ++kk) {
+                        const int k16 = h * (BN / 32) + kk;
+                        ptx::mma_ts_elect(tmem + col_o, tmem + col_s + k16 * 8, vd + ((k16 * 2048) >> 4),
+                                          IDESC_PV, (accumulate || k16 > 0) ? 1u : 0u);
                     }
                 }
                 return true;
