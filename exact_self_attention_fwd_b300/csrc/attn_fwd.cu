@@ -138,6 +138,8 @@ __device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abor
                           unsigned long long limit) {
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
+    // fast path: the phase has usually completed already
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     while (true) {
         const bool ok = ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS);
         if (__all_sync(0xffffffffu, ok)) return true;
