@@ -305,6 +305,72 @@ def run_reference(args, w: Workload):
     return 0
 
 
+def roofline_of(w: Workload, seconds_per_call: float, peaks: dict) -> dict:
+    """The bound that limits workload w on this chip and the fraction of it achieved.
+
+    Long sequences are tensor-core bound (FLOP/byte far above the ridge); the
+    short-sequence bidirectional workload is HBM bound."""
+    if w.name == "vit_base":
+        achieved = hbm_bytes(w) / seconds_per_call / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    achieved = flops(w) / seconds_per_call / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+
+
+def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
+    """Device time per attn_fwd call on workload w (seconds).
+
+    Calls of at least a few microseconds are timed one by one with CUDA events, a
+    256 MiB rewrite between them flushing L2. The tiny workload's call is shorter
+    than the host's launch overhead, so there a CUDA graph of `steps` calls is
+    replayed and timed as a whole (its 66 KB of inputs stay in L2)."""
+    import torch
+    q, k, v = make_qkv(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed + seed_offset, w.q_head0_scale)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call():
+        ea.attn_fwd(qd, kd, vd, causal=w.causal, window=w.window, scale=w.scale, out=out, lse=lse,
+                    stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize(dev)
+    if flops(w) < 1e8:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                ea.attn_fwd(qd, kd, vd, causal=w.causal, window=w.window, scale=w.scale, out=out,
+                            lse=lse, stream=torch.cuda.current_stream(dev))
+        g.replay()
+        torch.cuda.synchronize(dev)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        per = s0.elapsed_time(s1) / 1e3 / steps
+        return per, "CUDA graph of %d calls" % steps
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    per = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
+    return per, "per-call CUDA events, L2 flushed between calls"
+
+
 def run_ours(args, w: Workload):
     import torch
 
@@ -399,20 +465,22 @@ def run_ours(args, w: Workload):
     h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
 
+    # every workload of the suite, measured the same way (short runs, reported beside
+    # the headline; their launches are not counted in gpu_launches)
+    summary = {}
+    if args.summary_steps > 0:
+        peaks, _ = load_peaks()
+        for name, ww in WORKLOADS.items():
+            per, how = measure_workload(ea, ww, dev, args.summary_steps, 5, seed_offset=rank)
+            r = roofline_of(ww, per, peaks)
+            summary[name] = {"tflops": flops(ww) / per / 1e12, "us_per_call": per * 1e6,
+                             "gbs": hbm_bytes(ww) / per / 1e9, "bound": r["bound"],
+                             "frac": r["frac"], "timing": how}
+
     if rank == 0:
         peaks, peak_src = load_peaks()
         avg_s = local_total / args.steps
-        tensor_bound = w.name not in ("vit_base",)
-        if tensor_bound:
-            achieved = F / avg_s / 1e12
-            peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak}
-        else:
-            achieved = hbm_bytes(w) / avg_s / 1e9
-            peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-            roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak}
+        roof = roofline_of(w, avg_s, peaks)
         roof["traffic"] = recorded_traffic(w.name)
         roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
         roof["kernel"] = f"attn_fwd_kernel<{w.d}>"
@@ -435,6 +503,7 @@ def run_ours(args, w: Workload):
             "clocks": clocks,
             "stats_ms": {"mean": statistics.mean(per), "median": statistics.median(per),
                          "min": min(per), "trimmed_mean_70": statistics.mean(mid)},
+            "workloads": summary,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -453,6 +522,8 @@ def main(argv=None):
                     help="seconds of oracle work for the cpu_baseline field (0 = skip)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="total oracle seconds for --impl reference")
+    ap.add_argument("--summary-steps", type=int, default=100,
+                    help="calls per workload for the all-workload summary (0 = skip)")
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
     args = ap.parse_args(argv)
     if args.warmup < 3:
