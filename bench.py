@@ -471,10 +471,10 @@ def run_ours(args, w: Workload):
     if args.summary_steps > 0:
         peaks, _ = load_peaks()
         for name, ww in WORKLOADS.items():
-            per, how = measure_workload(ea, ww, dev, args.summary_steps, 5, seed_offset=rank)
-            r = roofline_of(ww, per, peaks)
-            summary[name] = {"tflops": flops(ww) / per / 1e12, "us_per_call": per * 1e6,
-                             "gbs": hbm_bytes(ww) / per / 1e9, "bound": r["bound"],
+            t_call, how = measure_workload(ea, ww, dev, args.summary_steps, 5, seed_offset=rank)
+            r = roofline_of(ww, t_call, peaks)
+            summary[name] = {"tflops": flops(ww) / t_call / 1e12, "us_per_call": t_call * 1e6,
+                             "gbs": hbm_bytes(ww) / t_call / 1e9, "bound": r["bound"],
                              "frac": r["frac"], "timing": how}
 
     if rank == 0:
