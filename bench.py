@@ -316,7 +316,9 @@ def roofline_of(w: Workload, seconds_per_call: float, peaks: dict) -> dict:
         return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
     achieved = flops(w) / seconds_per_call / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "frac_vs_sustained": achieved / sustained}
 
 
 def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
