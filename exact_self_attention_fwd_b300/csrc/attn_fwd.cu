@@ -186,6 +186,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     return w;
 }
 
+// The k-th unit of this CTA: rounds of gridDim.x units go to the CTAs in alternating
+// directions (0..G-1, then G-1..0), so a CTA that drew a heavy unit in one round draws
+// a light one in the next. Units are numbered heaviest first.
+__device__ __forceinline__ int snake_unit(int k) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 // KV tile range [lo, hi) that query tile starting at row q0 must visit; empty when
 // the tile lies past the end of the sequence. Tiles outside the range are fully
 // masked and never loaded.
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // elected lane.
             uint32_t kv_it = 0, q_it = 0, q_loads0 = 0, q_loads1 = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
                 const Unit w = decode_unit(u, p);
                 const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
                 int lo0, hi0, lo1, hi1;
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
 
-            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
                 const Unit w = decode_unit(u, p);
                 const int q0a = 2 * w.pair * BM;
                 int lo0, hi0, lo1, hi1;
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float sl2 = p.sl2;
         uint32_t s_use = 0, o_use = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+        for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
             const Unit w = decode_unit(u, p);
             const int q0 = (2 * w.pair + t) * BM;
             int lo, hi;
