@@ -97,12 +97,22 @@ struct Cfg {
     static constexpr int B_SFULL = 3 + 2 * STAGES;  // 2
     static constexpr int B_PFULL = B_SFULL + 2;     // 4: (tile, half of P)
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
-    static constexpr int B_DRAIN = B_OFULL + 2;     // 1
+    static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
+    static constexpr int B_PVDONE = B_SFREE + 2;    // 2: a P.V product of tile t completed
+    static constexpr int B_DRAIN = B_PVDONE + 2;    // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_CTL + 16;
     static constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;  // room to align to 1024 bytes
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
+    // Separate-P mode: when two S blocks, two O blocks and two 64-column P blocks fit in
+    // tensor memory (d = 64), P gets columns of its own. S_t(j+1) can then be computed as
+    // soon as the softmax warps have read S_t(j), while they are still turning it into
+    // P. Otherwise (d = 128) P overwrites the first half of its S block, and S_t(j+1)
+    // must wait until the P.V product of tile j has read P.
+    static constexpr bool SEP_P = (256 + 2 * D + 2 * 64) <= (int)TMEM_COLS;
+    static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
+    static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
@@ -249,6 +259,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(C::B_PFULL + 2 * t + 0), 4);  // one arrival per softmax warp
             ptx::mbar_init(bar(C::B_PFULL + 2 * t + 1), 4);
             ptx::mbar_init(bar(C::B_OFULL + t), 1);
+            ptx::mbar_init(bar(C::B_SFREE + t), 4);
+            ptx::mbar_init(bar(C::B_PVDONE + t), 1);
         }
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
@@ -341,6 +353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
             uint32_t kv_it = 0, q_use0 = 0, q_use1 = 0, p_use0 = 0, p_use1 = 0;
+            uint32_t sf_use0 = 0, sf_use1 = 0;
             bool ok = true;
 
             // S_t = Q_t K^T: K-major A and B, 16 columns of d per instruction. The
@@ -397,61 +410,119 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tc_fence_after();
                 int prev = -1;
                 uint32_t vprev = 0, vprev_ph = 0;
-                for (int j = lo; j < hi; ++j) {
-                    const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
-                    ++kv_it;
-                    const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
-                    ++kv_it;
-                    ok = wait_warp(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
-                    if (ok && prev >= 0) ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
+                if constexpr (C::SEP_P) {
+                    // S_t(j) is issued as soon as the softmax warps have read S_t(j-1);
+                    // then come the P.V products of key tile j-1 for both query tiles.
+                    auto pv_step = [&](int pj) -> bool {
+                        if (!wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit)) return false;
+                        ptx::tc_fence_after();
+                        if (pj >= lo0 && pj < hi0) {
+                            if (!issue_pv(0, C::COL_O0, C::COL_P0, vprev, pj > lo0, p_use0 & 1u)) return false;
+                            ++p_use0;
+                            ptx::mma_commit_elect(bar(pj == hi0 - 1 ? C::B_OFULL + 0 : C::B_PVDONE + 0));
+                        }
+                        if (has1 && pj >= lo1 && pj < hi1) {
+                            if (!issue_pv(1, C::COL_O1, C::COL_P1, vprev, pj > lo1, p_use1 & 1u)) return false;
+                            ++p_use1;
+                            ptx::mma_commit_elect(bar(pj == hi1 - 1 ? C::B_OFULL + 1 : C::B_PVDONE + 1));
+                        }
+                        ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
+                        return true;
+                    };
+                    for (int j = lo; j < hi; ++j) {
+                        const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        ok = wait_warp(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        if (j >= lo0 && j < hi0) {
+                            ok = wait_warp(bar(C::B_SFREE + 0), (sf_use0 & 1u) ^ 1u, abort_flag, limit);
+                            ++sf_use0;
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_s(qa0, C::COL_S0, ks);
+                            ptx::mma_commit_elect(bar(C::B_SFULL + 0));
+                        }
+                        if (has1 && j >= lo1 && j < hi1) {
+                            ok = wait_warp(bar(C::B_SFREE + 1), (sf_use1 & 1u) ^ 1u, abort_flag, limit);
+                            ++sf_use1;
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            issue_s(qa1, C::COL_S1, ks);
+                            ptx::mma_commit_elect(bar(C::B_SFULL + 1));
+                        }
+                        ptx::mma_commit_elect(bar(C::B_KVEMPTY + ks));
+                        if (prev >= 0) {
+                            ok = pv_step(prev);
+                            if (!ok) break;
+                        }
+                        prev = j;
+                        vprev = vs;
+                        vprev_ph = vph;
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                    ok = pv_step(prev);
+                    if (!ok) break;
+                } else {
+                    for (int j = lo; j < hi; ++j) {
+                        const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        const uint32_t vs = kv_it % C::STAGES, vph = (kv_it / C::STAGES) & 1u;
+                        ++kv_it;
+                        ok = wait_warp(bar(C::B_KVFULL + ks), kph, abort_flag, limit);
+                        if (ok && prev >= 0) ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
+                        if (prev >= lo0 && prev < hi0) {
+                            ok = issue_pv(0, C::COL_O0, C::COL_P0, vprev, prev > lo0, p_use0 & 1u);
+                            ++p_use0;
+                            if (!ok) break;
+                        }
+                        if (j >= lo0 && j < hi0) {
+                            issue_s(qa0, C::COL_S0, ks);
+                            ptx::mma_commit_elect(bar(C::B_SFULL + 0));
+                        }
+                        // tile 1: the same, overlapping softmax of tile 0
+                        if (has1 && prev >= lo1 && prev < hi1) {
+                            ok = issue_pv(1, C::COL_O1, C::COL_P1, vprev, prev > lo1, p_use1 & 1u);
+                            ++p_use1;
+                            if (!ok) break;
+                        }
+                        if (has1 && j >= lo1 && j < hi1) {
+                            issue_s(qa1, C::COL_S1, ks);
+                            ptx::mma_commit_elect(bar(C::B_SFULL + 1));
+                        }
+                        if (prev >= 0) ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
+                        ptx::mma_commit_elect(bar(C::B_KVEMPTY + ks));
+                        prev = j;
+                        vprev = vs;
+                        vprev_ph = vph;
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                    ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    // tile 0: O0 += P0(prev) V(prev), then S0 = Q0 K_j^T
                     if (prev >= lo0 && prev < hi0) {
-                        ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
+                        ok = issue_pv(0, C::COL_O0, C::COL_P0, vprev, prev > lo0, p_use0 & 1u);
                         ++p_use0;
                         if (!ok) break;
                     }
-                    if (j >= lo0 && j < hi0) {
-                        issue_s(qa0, C::COL_S0, ks);
-                        ptx::mma_commit_elect(bar(C::B_SFULL + 0));
+                    ptx::mma_commit_elect(bar(C::B_OFULL + 0));
+                    if (has1) {
+                        if (prev >= lo1 && prev < hi1) {
+                            ok = issue_pv(1, C::COL_O1, C::COL_P1, vprev, prev > lo1, p_use1 & 1u);
+                            ++p_use1;
+                            if (!ok) break;
+                        }
+                        ptx::mma_commit_elect(bar(C::B_OFULL + 1));
                     }
-                    // tile 1: the same, overlapping softmax of tile 0
-                    if (has1 && prev >= lo1 && prev < hi1) {
-                        ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
-                        ++p_use1;
-                        if (!ok) break;
-                    }
-                    if (has1 && j >= lo1 && j < hi1) {
-                        issue_s(qa1, C::COL_S1, ks);
-                        ptx::mma_commit_elect(bar(C::B_SFULL + 1));
-                    }
-                    if (prev >= 0) ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
-                    ptx::mma_commit_elect(bar(C::B_KVEMPTY + ks));
-                    prev = j;
-                    vprev = vs;
-                    vprev_ph = vph;
+                    ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
                 }
-                if (!ok) break;
-                ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
-                ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (prev >= lo0 && prev < hi0) {
-                    ok = issue_pv(0, C::COL_O0, C::COL_S0, vprev, prev > lo0, p_use0 & 1u);
-                    ++p_use0;
-                    if (!ok) break;
-                }
-                ptx::mma_commit_elect(bar(C::B_OFULL + 0));
-                if (has1) {
-                    if (prev >= lo1 && prev < hi1) {
-                        ok = issue_pv(1, C::COL_O1, C::COL_S1, vprev, prev > lo1, p_use1 & 1u);
-                        ++p_use1;
-                        if (!ok) break;
-                    }
-                    ptx::mma_commit_elect(bar(C::B_OFULL + 1));
-                }
-                ptx::mma_commit_elect(bar(C::B_KVEMPTY + vprev));
             }
             // every MMA this warp issued completes before tensor memory is freed
             ptx::mma_commit_elect(bar(C::B_DRAIN));
@@ -467,7 +538,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
+        const uint32_t t_p = tmem + lane_off + (t ? C::COL_P1 : C::COL_P0);
         const uint32_t bar_s = bar(C::B_SFULL + t), bar_o = bar(C::B_OFULL + t);
+        const uint32_t bar_sfree = bar(C::B_SFREE + t), bar_pvdone = bar(C::B_PVDONE + t);
+        uint32_t pv_w = 0;
         const uint32_t bar_p0 = bar(C::B_PFULL + 2 * t), bar_p1 = bar(C::B_PFULL + 2 * t + 1);
         const float sl2 = p.sl2;
         uint32_t s_use = 0, o_use = 0;
@@ -491,6 +565,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + 32 * c, sr[c]);
                 ptx::tmem_wait_ld();
+                if constexpr (C::SEP_P) {
+                    // S_t is in registers: the tensor core may overwrite it with S_t(j+1)
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar_sfree);
+                }
                 const int kv0 = j * BN;
                 if (block_needs_mask(p, q0, kv0)) {
 #pragma unroll
@@ -523,7 +603,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
                 // O <- alpha * O, only when some row of this warp raised its maximum; the
                 // first KV tile needs none (its PV product overwrites O). The previous PV
-                // product has completed: the S commit this warp waited for follows it.
+                // product must have completed: with P aliasing S, the S commit this warp
+                // waited for follows it; with separate P, wait for it here (this also
+                // frees the P block for this tile's P).
+                if constexpr (C::SEP_P) {
+                    if (j > lo) {
+                        ok = wait_warp(bar_pvdone, pv_w & 1u, abort_flag, limit);
+                        ++pv_w;
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                    }
+                }
                 if (j > lo && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -565,7 +655,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 ptx::add_bf16x2_halves(lr0, lr1, pk[e]);
                             }
                         }
-                        ptx::tmem_st16(t_s + 16 * c, pk);
+                        ptx::tmem_st16(t_p + 16 * c, pk);
                     }
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
