@@ -86,15 +86,18 @@ struct Cfg {
     static constexpr int CHUNK_BYTES = BM * 64 * 2;  // one 64-column, 128-byte-swizzled slab
     static constexpr int NCHUNK = D / 64;
     static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
+    // Q tiles of Q_BUFS units: with two, the producer loads the next unit's Q while the
+    // current unit still computes (d = 64, where shared memory has room for it).
+    static constexpr int Q_BUFS = (D == 64) ? 2 : 1;
     static constexpr int SMEM_Q = 0;
-    static constexpr int SMEM_KV = 2 * TILE_BYTES;
+    static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
     static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
     // barrier indices
-    static constexpr int B_QFULL = 0;               // 2
-    static constexpr int B_QEMPTY = 2;              // 1
-    static constexpr int B_KVFULL = 3;              // STAGES
-    static constexpr int B_KVEMPTY = 3 + STAGES;    // STAGES
-    static constexpr int B_SFULL = 3 + 2 * STAGES;  // 2
+    static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
+    static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
+    static constexpr int B_KVFULL = 3 * Q_BUFS;              // STAGES
+    static constexpr int B_KVEMPTY = B_KVFULL + STAGES;      // STAGES
+    static constexpr int B_SFULL = B_KVEMPTY + STAGES;       // 2
     static constexpr int B_PFULL = B_SFULL + 2;     // 4: (tile, half of P)
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
@@ -247,9 +250,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(C::B_QFULL + 0), 1);
-        ptx::mbar_init(bar(C::B_QFULL + 1), 1);
-        ptx::mbar_init(bar(C::B_QEMPTY), 1);
+        for (int b = 0; b < C::Q_BUFS; ++b) {
+            ptx::mbar_init(bar(C::B_QFULL + 2 * b + 0), 1);
+            ptx::mbar_init(bar(C::B_QFULL + 2 * b + 1), 1);
+            ptx::mbar_init(bar(C::B_QEMPTY + b), 1);
+        }
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar(C::B_KVFULL + s), 1);
             ptx::mbar_init(bar(C::B_KVEMPTY + s), 1);
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ============================================================ TMA producer
             // All 32 lanes run this loop with identical values; each copy is issued by one
             // elected lane.
-            uint32_t kv_it = 0, q_it = 0, q_loads0 = 0, q_loads1 = 0;
+            uint32_t kv_it = 0, q_it = 0;
             bool ok = true;
             for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
                 const Unit w = decode_unit(u, p);
@@ -301,22 +306,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int hi = has1 ? max(hi0, hi1) : hi0;
                 const int zq = w.b * p.Hq + w.hq;
                 const int zkv = w.b * p.Hkv + w.hkv;
-                ok = wait_warp(bar(C::B_QEMPTY), (q_it & 1u) ^ 1u, abort_flag, limit);
-                ++q_it;
+                // Q buffer of this unit; its previous contents (the unit Q_BUFS units
+                // back) are free once that unit's last S product has completed
+                const uint32_t qb = q_it % C::Q_BUFS, qph = (q_it / C::Q_BUFS) & 1u;
+                ok = wait_warp(bar(C::B_QEMPTY + qb), qph ^ 1u, abort_flag, limit);
                 if (!ok) break;
-                ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 0), C::TILE_BYTES);
+                ++q_it;
+                const uint32_t qdst = sb + C::SMEM_Q + qb * 2 * C::TILE_BYTES;
+                ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 2 * qb + 0), C::TILE_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::NCHUNK; ++c)
-                    ptx::tma_load_3d_elect(sb + C::SMEM_Q + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 0),
+                    ptx::tma_load_3d_elect(qdst + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 2 * qb + 0),
                                            c * 64, q0a, zq);
-                ++q_loads0;
                 if (has1) {
-                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 1), C::TILE_BYTES);
+                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 2 * qb + 1), C::TILE_BYTES);
 #pragma unroll
                     for (int c = 0; c < C::NCHUNK; ++c)
-                        ptx::tma_load_3d_elect(sb + C::SMEM_Q + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
-                                               bar(C::B_QFULL + 1), c * 64, q0b, zq);
-                    ++q_loads1;
+                        ptx::tma_load_3d_elect(qdst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
+                                               bar(C::B_QFULL + 2 * qb + 1), c * 64, q0b, zq);
+                } else if (lane == 0) {
+                    // no second tile: complete the phase anyway, so that both barriers of a
+                    // buffer always advance together
+                    ptx::mbar_arrive(bar(C::B_QFULL + 2 * qb + 1));
                 }
                 for (int j = lo; ok && j < hi; ++j) {
 #pragma unroll 1
@@ -342,8 +353,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t last = (kv_it - 1u - st) / C::STAGES * C::STAGES + st;
                     drain_wait(bar(C::B_KVFULL + st), (last / C::STAGES) & 1u, 100000000ull);
                 }
-                if (q_loads0) drain_wait(bar(C::B_QFULL + 0), (q_loads0 - 1u) & 1u, 100000000ull);
-                if (q_loads1) drain_wait(bar(C::B_QFULL + 1), (q_loads1 - 1u) & 1u, 100000000ull);
+                for (uint32_t b = 0; b < static_cast<uint32_t>(C::Q_BUFS); ++b) {
+                    const uint32_t n_b = (q_it + C::Q_BUFS - 1u - b) / C::Q_BUFS;  // loads into buffer b
+                    if (n_b == 0) continue;
+                    drain_wait(bar(C::B_QFULL + 2 * b + 0), (n_b - 1u) & 1u, 100000000ull);
+                    drain_wait(bar(C::B_QFULL + 2 * b + 1), (n_b - 1u) & 1u, 100000000ull);
+                }
             }
         } else if (warp == WARP_MMA) {
             // ============================================================ MMA issuer
@@ -352,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // elected lane.
             constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
-            uint32_t kv_it = 0, q_use0 = 0, q_use1 = 0, p_use0 = 0, p_use1 = 0;
+            uint32_t kv_it = 0, q_use = 0, p_use0 = 0, p_use1 = 0;
             uint32_t sf_use0 = 0, sf_use1 = 0;
             bool ok = true;
 
@@ -389,7 +404,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 return true;
             };
-            const uint32_t qa0 = sb + C::SMEM_Q, qa1 = sb + C::SMEM_Q + C::TILE_BYTES;
 
             for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
                 const Unit w = decode_unit(u, p);
@@ -400,12 +414,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool has1 = hi1 > lo1;
                 const int lo = has1 ? min(lo0, lo1) : lo0;
                 const int hi = has1 ? max(hi0, hi1) : hi0;
-                ok = wait_warp(bar(C::B_QFULL + 0), q_use0 & 1u, abort_flag, limit);
-                ++q_use0;
-                if (ok && has1) {
-                    ok = wait_warp(bar(C::B_QFULL + 1), q_use1 & 1u, abort_flag, limit);
-                    ++q_use1;
-                }
+                const uint32_t qb = q_use % C::Q_BUFS, qph = (q_use / C::Q_BUFS) & 1u;
+                ++q_use;
+                const uint32_t qa0 = sb + C::SMEM_Q + qb * 2 * C::TILE_BYTES, qa1 = qa0 + C::TILE_BYTES;
+                ok = wait_warp(bar(C::B_QFULL + 2 * qb + 0), qph, abort_flag, limit);
+                if (ok) ok = wait_warp(bar(C::B_QFULL + 2 * qb + 1), qph, abort_flag, limit);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 int prev = -1;
@@ -463,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         vprev_ph = vph;
                     }
                     if (!ok) break;
-                    ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                    ptx::mma_commit_elect(bar(C::B_QEMPTY + qb));  // Q tiles free once the last S is done
                     ok = pv_step(prev);
                     if (!ok) break;
                 } else {
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         vprev_ph = vph;
                     }
                     if (!ok) break;
-                    ptx::mma_commit_elect(bar(C::B_QEMPTY));  // Q tiles free once the last S is done
+                    ptx::mma_commit_elect(bar(C::B_QEMPTY + qb));  // Q tiles free once the last S is done
                     ok = wait_warp(bar(C::B_KVFULL + vprev), vprev_ph, abort_flag, limit);
                     if (!ok) break;
                     ptx::tc_fence_after();
@@ -573,14 +586,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const int kv0 = j * BN;
                 if (block_needs_mask(p, q0, kv0)) {
+                    // The keys row qi sees in this tile form one interval of columns
+                    // [c_lo, c_hi]: c_hi from the sequence end and the causal diagonal,
+                    // c_lo from the window. One unsigned compare per element against the
+                    // column index (a compile-time constant) keeps this rarely run block
+                    // small.
+                    const int c_hi = min(p.N - 1, p.causal ? qi : p.N - 1) - kv0;
+                    const int c_lo = p.window > 0 ? max(qi - p.window + 1 - kv0, 0) : 0;
+                    const uint32_t span = c_hi >= c_lo ? static_cast<uint32_t>(c_hi - c_lo) : 0u;
+                    const bool none = c_hi < c_lo;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const int kj = kv0 + c * 32 + e;
-                            const bool vis = (kj < p.N) && (!p.causal || kj <= qi) &&
-                                             (p.window == 0 || qi - kj < p.window);
-                            if (!vis) sr[c][e] = __float_as_uint(-INFINITY);
+                            const uint32_t off = static_cast<uint32_t>(c * 32 + e - c_lo);
+                            if (none || off > span) sr[c][e] = 0xFF800000u;  // -inf
                         }
                     }
                 }
