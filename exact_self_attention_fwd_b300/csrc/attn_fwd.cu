@@ -70,6 +70,29 @@ constexpr uint32_t WAIT_SLEEP_NS = 200000u;  // a waiting thread re-checks at le
 
 __device__ unsigned int g_status;  // bit 0: some wait ran out of time
 
+// Division of a non-negative int below 2^31 by an invariant divisor d >= 1, by a
+// multiply-high and a shift (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994, unsigned case): with l = ceil(log2 d) and
+// mul = floor(2^32 (2^l - d) / d) + 1, the quotient is (mulhi(mul, n) + n) >> l.
+// The sum stays below 2^32 because mulhi(mul, n) <= n < 2^31.
+struct FastDiv {
+    uint32_t mul, shift;
+};
+
+__host__ inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    FastDiv f;
+    f.mul = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1ull);
+    f.shift = l;
+    return f;
+}
+
+__device__ __forceinline__ int fdiv(int n, FastDiv f) {
+    const uint32_t un = static_cast<uint32_t>(n);
+    return static_cast<int>((__umulhi(un, f.mul) + un) >> f.shift);
+}
+
 struct Params {
     __nv_bfloat16 *o;
     float *lse;
@@ -78,6 +101,7 @@ struct Params {
     int n_pairs, n_kv, num_units;
     float sl2;  // scale * log2(e)
     unsigned long long timeout_ns;
+    FastDiv div_bh, div_hq, div_group;  // by B * Hq, Hq and Hq / Hkv
 };
 
 template <int D>
@@ -91,7 +115,10 @@ struct Cfg {
     static constexpr int Q_BUFS = (D == 64) ? 2 : 1;
     static constexpr int SMEM_Q = 0;
     static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
+    // one 64-column staging block per softmax warpgroup: O goes registers -> shared
+    // memory (128-byte-swizzled, like the TMA loads) -> global by a TMA tensor store
+    static constexpr int SMEM_STAGE = SMEM_KV + STAGES * TILE_BYTES;
+    static constexpr int SMEM_BAR = SMEM_STAGE + 2 * CHUNK_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
     static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
@@ -102,7 +129,9 @@ struct Cfg {
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
     static constexpr int B_PVDONE = B_SFREE + 2;    // 2: a P.V product of tile t completed
-    static constexpr int B_DRAIN = B_PVDONE + 2;    // 1
+    static constexpr int B_EFREE = B_PVDONE + 2;    // 2: staging block of tile t free
+    static constexpr int B_EFULL = B_EFREE + 2;     // 2: staging block of tile t written
+    static constexpr int B_DRAIN = B_EFULL + 2;     // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_CTL + 16;
@@ -188,14 +217,13 @@ struct Unit {
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
-    const int BH = p.B * p.Hq;
-    const int pr = u / BH;
-    const int bh = u - pr * BH;
+    const int pr = fdiv(u, p.div_bh);
+    const int bh = u - pr * (p.B * p.Hq);
     Unit w;
     w.pair = p.n_pairs - 1 - pr;
-    w.b = bh / p.Hq;
+    w.b = fdiv(bh, p.div_hq);
     w.hq = bh - w.b * p.Hq;
-    w.hkv = w.hq / p.group;
+    w.hkv = fdiv(w.hq, p.div_group);
     return w;
 }
 
@@ -236,7 +264,8 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const Params p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -266,6 +295,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(C::B_OFULL + t), 1);
             ptx::mbar_init(bar(C::B_SFREE + t), 4);
             ptx::mbar_init(bar(C::B_PVDONE + t), 1);
+            ptx::mbar_init(bar(C::B_EFREE + t), 1);
+            ptx::mbar_init(bar(C::B_EFULL + t), 4);
         }
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
@@ -275,6 +306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == WARP_MMA) {
         ptx::tmem_alloc(sb + C::SMEM_CTL, TMEM_COLS);
@@ -552,6 +584,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
         const uint32_t t_p = tmem + lane_off + (t ? C::COL_P1 : C::COL_P0);
+        uint8_t *stage_ptr = smem + C::SMEM_STAGE + t * C::CHUNK_BYTES;
+        const uint32_t stage_addr = sb + C::SMEM_STAGE + t * C::CHUNK_BYTES;
+        const bool store_thread = (quad == 0 && lane == 0);  // issues this warpgroup's O stores
+        const uint32_t bar_efree = bar(C::B_EFREE + t), bar_efull = bar(C::B_EFULL + t);
+        uint32_t e_use = 0;
         const uint32_t bar_s = bar(C::B_SFULL + t), bar_o = bar(C::B_OFULL + t);
         const uint32_t bar_sfree = bar(C::B_SFREE + t), bar_pvdone = bar(C::B_PVDONE + t);
         uint32_t pv_w = 0;
@@ -593,15 +630,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // small.
                     const int c_hi = min(p.N - 1, p.causal ? qi : p.N - 1) - kv0;
                     const int c_lo = p.window > 0 ? max(qi - p.window + 1 - kv0, 0) : 0;
-                    const uint32_t span = c_hi >= c_lo ? static_cast<uint32_t>(c_hi - c_lo) : 0u;
+                    // an empty interval becomes c_lo = -1, span = 0: every offset is > 0
                     const bool none = c_hi < c_lo;
+                    const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
+                    const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const uint32_t off = static_cast<uint32_t>(c * 32 + e - c_lo);
-                            if (none || off > span) sr[c][e] = 0xFF800000u;  // -inf
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            sr[c][e] = ptx::mask_above(sr[c][e], static_cast<uint32_t>(c * 32 + e) - base, span);
                     }
                 }
                 // row maximum: four independent chains of three-input max
@@ -690,17 +727,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ++o_use;
             if (!ok) break;
             ptx::tc_fence_after();
-            // epilogue: O / (sum of rounded P) -> bf16, and the natural-log LSE
+            // epilogue: O / (sum of rounded P) -> bf16 -> staging block -> TMA store (rows
+            // past the sequence end are clipped by the store), and the natural-log LSE
             const float inv_l = r_run > 0.f ? 1.f / r_run : 0.f;
             const size_t ridx = static_cast<size_t>(w.b * p.Hq + w.hq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
+            const int zq = w.b * p.Hq + w.hq;
+#pragma unroll 1
+            for (int h = 0; ok && h < D / 64; ++h) {
+                // the staging block is free once the previous store from it has read it
+                if (store_thread) {
+                    ptx::bulk_wait_group_read0();
+                    ptx::mbar_arrive(bar_efree);
+                }
+                ok = wait_warp(bar_efree, e_use & 1u, abort_flag, limit);
+                if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld32(t_o + 32 * c, r);
-                ptx::tmem_wait_ld();
-                if (qi < p.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D + 32 * c);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(t_o + 64 * h + 32 * c2, r);
+                    ptx::tmem_wait_ld();
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint4 val;
@@ -712,12 +758,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                  __uint_as_float(r[8 * g + 5]) * inv_l);
                         val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 6]) * inv_l,
                                                  __uint_as_float(r[8 * g + 7]) * inv_l);
-                        dst[g] = val;
+                        // 128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r % 8)
+                        const int chunk = (c2 * 4 + g) ^ (row & 7);
+                        *reinterpret_cast<uint4 *>(stage_ptr + row * 128 + chunk * 16) = val;
                     }
                 }
+                ptx::fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_efull);
+                if (quad == 0) {
+                    ok = wait_warp(bar_efull, e_use & 1u, abort_flag, limit);
+                    if (ok && store_thread) {
+                        ptx::tma_store_3d(&tm_o, stage_addr, 64 * h, q0, zq);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                ++e_use;
             }
+            if (!ok) break;
             if (qi < p.N) p.lse[ridx] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
         }
+        // the O stores read shared memory and write global memory after they are issued:
+        // both must be done before the CTA exits
+        if (store_thread) ptx::bulk_wait_group0();
     }
 
     ptx::tc_fence_before();
@@ -865,11 +928,12 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
            int N, int causal, int window, float scale, cudaStream_t stream, int sms) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     int rc;
     if ((rc = encode_map(enc, &mq, q, D, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mk, k, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mo, o, D, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     attn::Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
@@ -885,8 +949,11 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     p.num_units = B * Hq * p.n_pairs;
     p.sl2 = scale * 1.4426950408889634f;
     p.timeout_ns = attn::WAIT_LIMIT_NS;
+    p.div_bh = attn::make_fastdiv(static_cast<uint32_t>(B * Hq));
+    p.div_hq = attn::make_fastdiv(static_cast<uint32_t>(Hq));
+    p.div_group = attn::make_fastdiv(static_cast<uint32_t>(p.group));
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+    attn::attn_fwd_kernel<D><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;

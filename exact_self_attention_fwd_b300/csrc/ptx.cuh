@@ -78,6 +78,30 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 3-D tiled tensor copy shared -> global (rows and columns outside the tensor are not
+// written), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until every bulk group this thread committed has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until every bulk group this thread committed has completed
+__device__ __forceinline__ void bulk_wait_group0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// make this thread's generic-proxy shared-memory writes visible to the async proxy
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -270,6 +294,16 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// v, or the bit pattern of -inf when off > span (unsigned), as one predicated select
+__device__ __forceinline__ uint32_t mask_above(uint32_t v, uint32_t off, uint32_t span) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p;\n\t"
+        "setp.gt.u32 p, %1, %2;\n\t"
+        "selp.b32 %0, 0xFF800000, %3, p;\n\t}"
+        : "=r"(r) : "r"(off), "r"(span), "r"(v));
+    return r;
 }
 
 // max of three floats in one instruction
