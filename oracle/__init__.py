@@ -44,13 +44,14 @@ def _declare(lib):
     f64p = ctypes.POINTER(ctypes.c_double)
     i64p = ctypes.POINTER(ctypes.c_int64)
     i64 = ctypes.c_int64
+    i32p = ctypes.POINTER(ctypes.c_int32)
     lib.attn_ref_fwd_rows_f64.argtypes = [
         u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
-        i64p, i64, f64p, f64p, ctypes.c_int]
+        i32p, i64p, i64, f64p, f64p, ctypes.c_int]
     lib.attn_ref_fwd_rows_f64.restype = ctypes.c_int
     lib.attn_ref_fwd_f64.argtypes = [
         u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
-        f64p, f64p, ctypes.c_int]
+        i32p, f64p, f64p, ctypes.c_int]
     lib.attn_ref_fwd_f64.restype = ctypes.c_int
     return lib
 
@@ -87,10 +88,12 @@ def _as_bits(x) -> np.ndarray:
 
 
 def attn_ref_rows(q, k, v, causal: bool, window: int, scale: float, rows=None,
-                  nthreads: int | None = None, lib=None):
+                  nthreads: int | None = None, lib=None, key_len=None):
     """fp64 O and LSE for the listed flat rows ((b*Hq)+hq)*N + i (all rows if None).
 
-    q: [B,Hq,N,d], k/v: [B,Hkv,N,d] bf16. Returns (o [nrows,d] f64, lse [nrows] f64).
+    q: [B,Hq,N,d], k/v: [B,Hkv,N,d] bf16; key_len: optional per-batch valid length
+    (right padding). Returns (o [nrows,d] f64, lse [nrows] f64); a row with no visible
+    key has o = 0 and lse = -inf.
     """
     qb, kb, vb = _as_bits(q), _as_bits(k), _as_bits(v)
     B, Hq, N, d = qb.shape
@@ -103,6 +106,11 @@ def attn_ref_rows(q, k, v, causal: bool, window: int, scale: float, rows=None,
     else:
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         nrows = rows_arr.size
+    kl = None
+    if key_len is not None:
+        kl = np.ascontiguousarray(np.asarray(key_len, dtype=np.int32).reshape(-1))
+        if kl.size != B:
+            raise ValueError("key_len must have one entry per batch")
     o = np.empty((nrows, d), dtype=np.float64)
     lse = np.empty((nrows,), dtype=np.float64)
     L = lib or load()
@@ -111,6 +119,7 @@ def attn_ref_rows(q, k, v, causal: bool, window: int, scale: float, rows=None,
     rc = L.attn_ref_fwd_rows_f64(
         qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p),
         B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+        kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
         rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
         nrows, o.ctypes.data_as(f64p), lse.ctypes.data_as(f64p),
         int(nthreads or default_threads()))
@@ -120,11 +129,11 @@ def attn_ref_rows(q, k, v, causal: bool, window: int, scale: float, rows=None,
 
 
 def attn_ref(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
-             nthreads: int | None = None, lib=None):
+             nthreads: int | None = None, lib=None, key_len=None):
     """fp64 O [B,Hq,N,d] and LSE [B,Hq,N] for every row."""
     qb = _as_bits(q)
     B, Hq, N, d = qb.shape
     if scale is None:
         scale = 1.0 / float(np.sqrt(d))
-    o, lse = attn_ref_rows(qb, k, v, causal, window, scale, None, nthreads, lib)
+    o, lse = attn_ref_rows(qb, k, v, causal, window, scale, None, nthreads, lib, key_len)
     return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)

@@ -9,7 +9,11 @@
  *
  *   For every batch b, query head hq and query row i:
  *     kv     = hq / (Hq / Hkv)                     grouped-query head map
- *     J(i)   = { j in [0,N) : (!causal || j <= i) && (window == 0 || i - j < window) }
+ *     L      = key_len ? key_len[b] : N            valid (unpadded) length of batch b
+ *     J(i)   = { j in [0,N) : i < L && j < L
+ *                             && (!causal || j <= i)
+ *                             && (window == 0 || i - j < window)
+ *                             && (window == 0 || causal || j - i < window) }
  *     s_ij   = scale * sum_c q[b,hq,i,c] * k[b,kv,j,c]        for j in J(i)
  *     m_i    = max_j s_ij
  *     lse_i  = m_i + ln( sum_j exp(s_ij - m_i) )             natural-log log-sum-exp
@@ -28,7 +32,15 @@
  *   - grouped-query attention and sliding-window attention are named as compared
  *     variants on the "Attentions Under the Microscope" summary (gist.science),
  *     section "방법론". The head map kv = hq / G (consecutive groups) and the window
- *     rule i - j < window are the plainest readings; the pages fix neither.
+ *     rule i - j < window are the plainest readings; the pages fix neither. Without
+ *     the look-ahead mask the window is read symmetrically, |i - j| < window (the
+ *     local window of Longformer-style sparse attention, devhandbook.co.kr table
+ *     "2. Attention 메커니즘 최적화 기법 비교").
+ *   - padding: padding tokens neither give nor receive attention, their scores being
+ *     set to -inf (palettepath-it.com guide, "패딩 마스킹 (Padding Masking)"); with
+ *     per-token validity as in the blog's variable-length example (devhandbook.co.kr,
+ *     "Example 7"), read as right padding: batch b's first key_len[b] tokens are
+ *     valid. A padded query row therefore has no visible key.
  *
  * Inputs are bf16 bit patterns (uint16); each is widened exactly to fp64.
  * A row whose visible set is empty (impossible for valid arguments, since j = i is
@@ -47,9 +59,11 @@ static double bf16_bits_to_double(uint16_t h) {
     return (double)f;
 }
 
-static int key_visible(int64_t i, int64_t j, int causal, int64_t window) {
+static int key_visible(int64_t i, int64_t j, int causal, int64_t window, int64_t L) {
+    if (i >= L || j >= L) return 0;
     if (causal && j > i) return 0;
     if (window > 0 && i - j >= window) return 0;
+    if (window > 0 && !causal && j - i >= window) return 0;
     return 1;
 }
 
@@ -59,6 +73,7 @@ typedef struct {
     int causal;
     int64_t window;
     double scale;
+    const int32_t *key_len; /* valid length per batch, or NULL (all N valid) */
     const int64_t *rows; /* flat row ids ((b*Hq)+hq)*N + i, or NULL for all rows */
     int64_t row_begin, row_end;
     double *o, *lse;     /* o: one d-vector per requested row; lse: one per row */
@@ -74,6 +89,9 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
     const int64_t b = bh / jb->Hq;
     const int64_t group = jb->Hq / jb->Hkv;
     const int64_t kv = hq / group;
+    int64_t L = jb->key_len ? (int64_t)jb->key_len[b] : N;
+    if (L < 0) L = 0;
+    if (L > N) L = N;
 
     const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;
     const uint16_t *kbase = jb->k + (b * jb->Hkv + kv) * N * d;
@@ -85,7 +103,7 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
     double m = -INFINITY;
     int64_t nvis = 0;
     for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
         const uint16_t *krow = kbase + j * d;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c) dot += qd[c] * bf16_bits_to_double(krow[c]);
@@ -102,7 +120,7 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
     /* log-sum-exp */
     double l = 0.0;
     for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
         l += exp(s[j] - m);
     }
     const double lse = m + log(l);
@@ -110,7 +128,7 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
 
     /* probability-weighted sum of value rows */
     for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window)) continue;
+        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
         const double p = exp(s[j] - lse);
         const uint16_t *vrow = vbase + j * d;
         for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_bits_to_double(vrow[c]);
@@ -137,7 +155,6 @@ static int check_args(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return -3;
     if (Hq % Hkv != 0) return -3;
     if (window < 0) return -3;
-    if (window > 0 && !causal) return -4;
     if (!(scale > 0.0) || !isfinite(scale)) return -3;
     return 0;
 }
@@ -150,7 +167,7 @@ static int check_args(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
  */
 int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                           int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
-                          int causal, int64_t window, double scale,
+                          int causal, int64_t window, double scale, const int32_t *key_len,
                           const int64_t *rows, int64_t nrows, double *o, double *lse,
                           int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
@@ -178,6 +195,7 @@ int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *
         jb->q = q; jb->k = k; jb->v = v;
         jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d;
         jb->causal = causal; jb->window = window; jb->scale = scale;
+        jb->key_len = key_len;
         jb->rows = rows;
         jb->row_begin = nrows * t / nthreads;
         jb->row_end = nrows * (t + 1) / nthreads;
@@ -197,11 +215,11 @@ int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *
     return 0;
 }
 
-/* All rows: o is [B,Hq,N,d], lse is [B,Hq,N], both fp64. */
+/* All rows: o is [B,Hq,N,d], lse is [B,Hq,N], both fp64. key_len may be NULL. */
 int attn_ref_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
-                     int causal, int64_t window, double scale,
+                     int causal, int64_t window, double scale, const int32_t *key_len,
                      double *o, double *lse, int nthreads) {
-    return attn_ref_fwd_rows_f64(q, k, v, B, Hq, Hkv, N, d, causal, window, scale,
+    return attn_ref_fwd_rows_f64(q, k, v, B, Hq, Hkv, N, d, causal, window, scale, key_len,
                                  NULL, B * Hq * N, o, lse, nthreads);
 }

@@ -17,6 +17,10 @@ What pins what:
   permutation       bidirectional O, LSE invariant under a joint permutation of K, V rows
   brute force       mpmath at 40 digits on a small random case (O and LSE)
   library           torch CPU fp64 scaled_dot_product_attention with a boolean mask
+  padding           zero-query closed form with per-batch valid lengths (padded rows
+                    see nothing); valid rows equal the batch truncated to its length
+  symmetric window  one-hot closed form for |i - j| < W; W >= N equals bidirectional;
+                    brute force and torch SDPA with padding and both window kinds
 """
 from __future__ import annotations
 
@@ -44,9 +48,16 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def _close(a, b, tol, what):
+    """max |a - b| / max(1, |b|) <= tol; equal infinities match, NaN never does."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
-    err = np.max(np.abs(a - b) / np.maximum(1.0, np.abs(b))) if a.size else 0.0
+    if not a.size:
+        return
+    assert not (np.isnan(a).any() or np.isnan(b).any()), f"{what}: NaN"
+    finite = np.isfinite(a) & np.isfinite(b)
+    with np.errstate(invalid="ignore", over="ignore"):
+        rel = np.abs(a - b) / np.maximum(1.0, np.abs(b))
+    err = np.where(a == b, 0.0, np.where(finite, rel, np.inf)).max()
     assert err <= tol, f"{what}: max rel err {err:.3e} > {tol:.1e}"
 
 
@@ -269,5 +280,157 @@ def pin_torch_sdpa(lib):
             _close(o, ref.numpy(), 1e-12, f"torch SDPA causal={causal} W={W}")
 
 
+# ---------------------------------------------------------------- padding and symmetric window
+def _visible(i, j, causal, W, L):
+    """The mask, restated from the pages for the pins below (right padding to L)."""
+    if i >= L or j >= L:
+        return False
+    if causal and j > i:
+        return False
+    if W and i - j >= W:
+        return False
+    if W and not causal and j - i >= W:
+        return False
+    return True
+
+
+def pin_padding_zero_query(lib):
+    # all scores equal: a valid row averages the V rows it sees, lse = ln(count); a
+    # padded row sees nothing (o = 0, lse = -inf)
+    g = torch.Generator().manual_seed(21)
+    B, N, d = 3, 23, 8
+    q = torch.zeros(B, 2, N, d, dtype=torch.bfloat16)
+    k = torch.randn(B, 1, N, d, generator=g).bfloat16()
+    v = torch.randn(B, 1, N, d, generator=g).bfloat16()
+    vd = f64(v)
+    key_len = [0, 9, N]
+    for causal, W in [(False, 0), (True, 0), (True, 4), (False, 3), (False, 40)]:
+        o, lse = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=0.7, lib=lib, key_len=key_len)
+        for b in range(B):
+            for h in range(2):
+                for i in range(N):
+                    js = [j for j in range(N) if _visible(i, j, causal, W, key_len[b])]
+                    if not js:
+                        assert lse[b, h, i] == -np.inf and not o[b, h, i].any(), "padded row"
+                        continue
+                    _close(lse[b, h, i], math.log(len(js)), 1e-13, f"pad zero-q lse b={b} i={i}")
+                    _close(o[b, h, i], vd[b, 0, js].mean(axis=0), 1e-13, f"pad zero-q O b={b} i={i}")
+
+
+def pin_padding_truncation(lib):
+    # the valid rows of a padded batch equal attention over that batch truncated to its
+    # valid length, with no padding at all
+    g = torch.Generator().manual_seed(22)
+    B, Hq, Hkv, N, d = 3, 4, 2, 29, 16
+    q = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    k = torch.randn(B, Hkv, N, d, generator=g).bfloat16()
+    v = torch.randn(B, Hkv, N, d, generator=g).bfloat16()
+    key_len = [29, 1, 17]
+    for causal, W in [(False, 0), (True, 0), (True, 5), (False, 6)]:
+        o, lse = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=0.3, lib=lib, key_len=key_len)
+        for b, L in enumerate(key_len):
+            ot, lt = oracle.attn_ref(q[b:b + 1, :, :L].contiguous(), k[b:b + 1, :, :L].contiguous(),
+                                     v[b:b + 1, :, :L].contiguous(), causal=causal, window=W, scale=0.3,
+                                     lib=lib)
+            _close(o[b, :, :L], ot[0], 1e-13, f"truncation O b={b}")
+            _close(lse[b, :, :L], lt[0], 1e-13, f"truncation lse b={b}")
+            assert np.all(lse[b, :, L:] == -np.inf) and not o[b, :, L:].any()
+
+
+def pin_symmetric_window_one_hot(lib):
+    # the one-hot closed form with a symmetric window: row i sees keys
+    # max(0, i-W+1) .. min(N-1, i+W-1)
+    N, d = 8, 4
+    a, bb = 2.0, 1.5
+    scale = 0.5
+    c = scale * a * bb
+    q = bf16([[a if col == i % 4 else 0.0 for col in range(d)] for i in range(N)])
+    k = bf16([[bb if col == j % 4 else 0.0 for col in range(d)] for j in range(N)])
+    v = bf16([[3.0 if col == (j + 1) % 4 else 0.0 for col in range(d)] for j in range(N)])
+    for W in (1, 2, 3, 5, 8, 20):
+        o, lse = oracle.attn_ref(q.reshape(1, 1, N, d), k.reshape(1, 1, N, d), v.reshape(1, 1, N, d),
+                                 causal=False, window=W, scale=scale, lib=lib)
+        for i in range(N):
+            lo, hi = max(0, i - W + 1), min(N - 1, i + W - 1)
+            cnt = [_count_residue(lo, hi, r) for r in range(4)]
+            ri = i % 4
+            Z = cnt[ri] * math.exp(c) + (sum(cnt) - cnt[ri])
+            o_cf = [0.0] * d
+            for r in range(4):
+                w = (math.exp(c) if r == ri else 1.0) * cnt[r]
+                o_cf[(r + 1) % 4] += 3.0 * w / Z
+            _close(lse[0, 0, i], math.log(Z), 1e-13, f"sym one-hot lse W={W} i={i}")
+            _close(o[0, 0, i], o_cf, 1e-13, f"sym one-hot O W={W} i={i}")
+
+
+def pin_symmetric_window_ge_n(lib):
+    g = torch.Generator().manual_seed(23)
+    q = torch.randn(1, 2, 31, 8, generator=g).bfloat16()
+    k = torch.randn(1, 2, 31, 8, generator=g).bfloat16()
+    v = torch.randn(1, 2, 31, 8, generator=g).bfloat16()
+    o0, l0 = oracle.attn_ref(q, k, v, scale=0.4, lib=lib)
+    for W in (31, 32, 500):
+        o1, l1 = oracle.attn_ref(q, k, v, causal=False, window=W, scale=0.4, lib=lib)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1), f"symmetric window {W} >= N"
+    o1, _ = oracle.attn_ref(q, k, v, causal=False, window=30, scale=0.4, lib=lib)
+    assert not np.array_equal(o0, o1)
+
+
+def pin_masks_brute_force(lib):
+    import mpmath
+    mpmath.mp.dps = 40
+    g = torch.Generator().manual_seed(24)
+    B, Hq, Hkv, N, d = 2, 2, 1, 11, 4
+    q = (2 * torch.randn(B, Hq, N, d, generator=g)).bfloat16()
+    k = (2 * torch.randn(B, Hkv, N, d, generator=g)).bfloat16()
+    v = torch.randn(B, Hkv, N, d, generator=g).bfloat16()
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    scale = 0.5
+    key_len = [7, 11]
+    for causal, W in [(False, 3), (True, 2), (False, 0)]:
+        o, lse = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=scale, lib=lib, key_len=key_len)
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(N):
+                    js = [j for j in range(N) if _visible(i, j, causal, W, key_len[b])]
+                    if not js:
+                        assert lse[b, h, i] == -np.inf
+                        continue
+                    s = {j: mpmath.mpf(scale) * mpmath.fsum(mpmath.mpf(qd[b, h, i, cc]) * mpmath.mpf(kd[b, 0, j, cc])
+                                                           for cc in range(d)) for j in js}
+                    z = mpmath.fsum(mpmath.exp(s[j]) for j in js)
+                    _close(lse[b, h, i], float(mpmath.log(z)), 1e-13, "masks brute-force lse")
+                    ob = [float(mpmath.fsum(mpmath.exp(s[j]) * mpmath.mpf(vd[b, 0, j, cc]) for j in js) / z)
+                          for cc in range(d)]
+                    _close(o[b, h, i], ob, 1e-13, "masks brute-force O")
+
+
+def pin_masks_torch_sdpa(lib):
+    import torch.nn.functional as F
+    g = torch.Generator().manual_seed(25)
+    B, H, N, d = 2, 2, 70, 32
+    q = torch.randn(B, H, N, d, generator=g).bfloat16()
+    k = torch.randn(B, H, N, d, generator=g).bfloat16()
+    v = torch.randn(B, H, N, d, generator=g).bfloat16()
+    key_len = [70, 45]
+    i = torch.arange(N).view(N, 1)
+    j = torch.arange(N).view(1, N)
+    for causal, W in [(False, 9), (False, 0), (True, 13)]:
+        o, _ = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=0.2, lib=lib, key_len=key_len)
+        for b, L in enumerate(key_len):
+            mask = (i < L) & (j < L)
+            if causal:
+                mask &= j <= i
+            if W:
+                mask &= (i - j) < W
+                if not causal:
+                    mask &= (j - i) < W
+            ref = F.scaled_dot_product_attention(q[b:b + 1].double(), k[b:b + 1].double(), v[b:b + 1].double(),
+                                                 attn_mask=mask, scale=0.2)
+            _close(o[b, :, :L], ref[0, :, :L].numpy(), 1e-12, f"torch SDPA masks b={b} c={causal} W={W}")
+
+
 ALL_PINS = [pin_worked_example, pin_one_hot, pin_zero_query, pin_constant_v, pin_causal_row0,
-            pin_gqa, pin_window_ge_n, pin_permutation, pin_brute_force, pin_torch_sdpa]
+            pin_gqa, pin_window_ge_n, pin_permutation, pin_brute_force, pin_torch_sdpa,
+            pin_padding_zero_query, pin_padding_truncation, pin_symmetric_window_one_hot,
+            pin_symmetric_window_ge_n, pin_masks_brute_force, pin_masks_torch_sdpa]

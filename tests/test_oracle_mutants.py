@@ -29,6 +29,15 @@ MUTANTS = {
     # wrong query row index (row-major stride slip)
     "query_row_index": ("const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;",
                         "const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i / 2) * d;"),
+    # padded query rows are not masked (only padded keys are)
+    "padding_rows_unmasked": ("if (i >= L || j >= L) return 0;", "if (j >= L) return 0;"),
+    # padded keys are not masked
+    "padding_keys_unmasked": ("if (i >= L || j >= L) return 0;", "if (i >= L) return 0;"),
+    # the symmetric window forgets its right edge
+    "symmetric_window_one_sided": ("if (window > 0 && !causal && j - i >= window) return 0;", ""),
+    # the symmetric window's right edge is off by one
+    "symmetric_window_off_by_one": ("if (window > 0 && !causal && j - i >= window) return 0;",
+                                    "if (window > 0 && !causal && j - i > window) return 0;"),
     # value accumulation misses the probability weight normalisation
     "unnormalised_output": ("const double p = exp(s[j] - lse);", "const double p = exp(s[j] - m);"),
 }

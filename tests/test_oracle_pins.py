@@ -40,8 +40,7 @@ def test_thread_count_does_not_change_result(lib):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(window=-1, causal=True), dict(window=4, causal=False), dict(scale=0.0),
-    dict(scale=float("nan")),
+    dict(window=-1, causal=True), dict(scale=0.0), dict(scale=float("nan")),
 ])
 def test_rejects_bad_arguments(lib, bad):
     q = torch.zeros(1, 1, 4, 8, dtype=torch.bfloat16)
