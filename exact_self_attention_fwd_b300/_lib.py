@@ -44,6 +44,8 @@ def _declare(lib):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd.restype = i
+    lib.attn_fwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_fwd_padded.restype = i
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_host.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -109,9 +111,10 @@ def _check_tensors(q, k, v):
 
 
 def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
-             out=None, lse=None, stream=None):
+             out=None, lse=None, stream=None, key_len=None):
     """O [B,Hq,N,d] bf16 and LSE [B,Hq,N] fp32 for CUDA bf16 q [B,Hq,N,d], k/v [B,Hkv,N,d].
 
+    key_len: optional CUDA int32 [B] of valid lengths (right padding; attn_fwd_padded).
     Asynchronous on `stream` (default: the current stream of q's device).
     """
     import torch
@@ -130,10 +133,20 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
     if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != dev:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, Hq, N]")
     L = load()
+    if key_len is not None:
+        if (key_len.device != dev or key_len.dtype != torch.int32 or key_len.numel() != B
+                or not key_len.is_contiguous()):
+            raise ValueError("key_len must be a contiguous int32 CUDA tensor with B entries")
     with torch.cuda.device(dev):
-        rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                        B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
-                        _stream_handle(stream, dev))
+        if key_len is None:
+            rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+                            _stream_handle(stream, dev))
+        else:
+            rc = L.attn_fwd_padded(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), key_len.data_ptr(), B, Hq, Hkv, N, d,
+                                   int(bool(causal)), int(window), float(scale),
+                                   _stream_handle(stream, dev))
     _check(rc)
     return out, lse
 

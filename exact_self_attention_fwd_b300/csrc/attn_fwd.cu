@@ -96,8 +96,10 @@ __device__ __forceinline__ int fdiv(int n, FastDiv f) {
 struct Params {
     __nv_bfloat16 *o;
     float *lse;
+    const int *key_len;  // valid (unpadded) length per batch, or null: all N valid
     int B, Hq, Hkv, N, group;
-    int causal, window;
+    int causal, window;  // window 0 = none (a window >= N is passed as 0)
+    int sym;             // window without the look-ahead mask: |i - j| < window
     int n_pairs, n_kv, num_units;
     float sl2;  // scale * log2(e)
     unsigned long long timeout_ns;
@@ -238,13 +240,30 @@ __device__ __forceinline__ int snake_unit(int k) {
 // KV tile range [lo, hi) that query tile starting at row q0 must visit; empty when
 // the tile lies past the end of the sequence. Tiles outside the range are fully
 // masked and never loaded.
-__device__ __forceinline__ void tile_range(const Params &p, int q0, int &lo, int &hi) {
+// Valid length of batch b: key_len[b] clamped to [0, N], or N without padding.
+__device__ __forceinline__ int valid_len(const Params &p, int b) {
+    if (!p.key_len) return p.N;
+    return min(max(__ldg(p.key_len + b), 0), p.N);
+}
+
+// Row i of a batch with valid length L sees the keys j of one interval:
+//   i >= L (a padded row): none
+//   otherwise j <= min(L - 1, causal ? i : N - 1, symmetric window ? i + W - 1 : N - 1)
+//   and       j >= (window ? i - W + 1 : 0)
+// Both ends grow with i, so the KV tiles a query tile needs are those between the
+// first row's lower end and the last valid row's upper end; tiles outside are fully
+// masked and never loaded. An empty range means every row of the tile is padding.
+__device__ __forceinline__ void tile_range(const Params &p, int q0, int L, int &lo, int &hi) {
     lo = 0;
     hi = 0;
-    if (q0 >= p.N) return;
-    // the tile's last row q0 + BM - 1 sees keys up to itself (BM == BN)
-    hi = p.causal ? min(p.n_kv, q0 / BN + 1) : p.n_kv;
-    if (p.causal && p.window > 0) {
+    const int rows_end = min(L, q0 + BM);  // valid rows are [q0, rows_end)
+    if (q0 >= rows_end) return;
+    const int r_last = rows_end - 1;
+    int last_key = L - 1;
+    if (p.causal) last_key = min(last_key, r_last);
+    if (p.sym) last_key = min(last_key, r_last + p.window - 1);
+    hi = last_key / BN + 1;
+    if (p.window > 0) {
         const int first = q0 - p.window + 1;  // first visible key of row q0
         lo = first > 0 ? first / BN : 0;
     }
@@ -252,10 +271,12 @@ __device__ __forceinline__ void tile_range(const Params &p, int q0, int &lo, int
 
 // a (query tile, key tile) block needs element masking when it crosses the end of
 // the sequence, the causal diagonal or the window edge
-__device__ __forceinline__ bool block_needs_mask(const Params &p, int q0, int kv0) {
-    if (kv0 + BN > p.N) return true;
-    if (p.causal && kv0 + BN - 1 > q0) return true;
-    if (p.window > 0 && (q0 + BM - 1) - kv0 >= p.window) return true;
+__device__ __forceinline__ bool block_needs_mask(const Params &p, int q0, int kv0, int L) {
+    if (kv0 + BN > L) return true;                                     // keys past the valid end
+    if (L < p.N && q0 + BM > L) return true;                           // padded query rows
+    if (p.causal && kv0 + BN - 1 > q0) return true;                    // the diagonal
+    if (p.window > 0 && (q0 + BM - 1) - kv0 >= p.window) return true;  // the window's lower edge
+    if (p.sym && kv0 + BN - 1 > q0 + p.window - 1) return true;        // the upper edge
     return false;
 }
 
@@ -331,8 +352,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Unit w = decode_unit(u, p);
                 const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
                 int lo0, hi0, lo1, hi1;
-                tile_range(p, q0a, lo0, hi0);
-                tile_range(p, q0b, lo1, hi1);
+                const int L = valid_len(p, w.b);
+                tile_range(p, q0a, L, lo0, hi0);
+                tile_range(p, q0b, L, lo1, hi1);
+                // a first tile without visible keys has only padded rows, and so has the
+                // second: nothing to load (the softmax warps write the zero output)
+                if (hi0 <= lo0) continue;
                 const bool has1 = hi1 > lo1;
                 const int lo = has1 ? min(lo0, lo1) : lo0;
                 const int hi = has1 ? max(hi0, hi1) : hi0;
@@ -441,8 +466,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Unit w = decode_unit(u, p);
                 const int q0a = 2 * w.pair * BM;
                 int lo0, hi0, lo1, hi1;
-                tile_range(p, q0a, lo0, hi0);
-                tile_range(p, q0a + BM, lo1, hi1);
+                const int L = valid_len(p, w.b);
+                tile_range(p, q0a, L, lo0, hi0);
+                tile_range(p, q0a + BM, L, lo1, hi1);
+                if (hi0 <= lo0) continue;  // padding only: nothing to compute
                 const bool has1 = hi1 > lo1;
                 const int lo = has1 ? min(lo0, lo1) : lo0;
                 const int hi = has1 ? max(hi0, hi1) : hi0;
@@ -600,8 +627,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const Unit w = decode_unit(u, p);
             const int q0 = (2 * w.pair + t) * BM;
             int lo, hi;
-            tile_range(p, q0, lo, hi);
-            if (hi <= lo) continue;
+            if (q0 >= p.N) continue;  // no rows in this tile
+            const int L = valid_len(p, w.b);
+            tile_range(p, q0, L, lo, hi);
+            const bool empty = hi <= lo;  // all rows padded: the output is zero
             const int qi = q0 + row;
             float m_run = -INFINITY;  // running max of scale*s*log2(e)
             float l_run = 0.f;        // running sum of 2^(x - m_run), for the LSE
@@ -622,16 +651,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) ptx::mbar_arrive(bar_sfree);
                 }
                 const int kv0 = j * BN;
-                if (block_needs_mask(p, q0, kv0)) {
+                if (block_needs_mask(p, q0, kv0, L)) {
                     // The keys row qi sees in this tile form one interval of columns
                     // [c_lo, c_hi]: c_hi from the sequence end and the causal diagonal,
                     // c_lo from the window. One unsigned compare per element against the
                     // column index (a compile-time constant) keeps this rarely run block
                     // small.
-                    const int c_hi = min(p.N - 1, p.causal ? qi : p.N - 1) - kv0;
+                    int c_hi = L - 1;
+                    if (p.causal) c_hi = min(c_hi, qi);
+                    if (p.sym) c_hi = min(c_hi, qi + p.window - 1);
+                    c_hi -= kv0;
                     const int c_lo = p.window > 0 ? max(qi - p.window + 1 - kv0, 0) : 0;
-                    // an empty interval becomes c_lo = -1, span = 0: every offset is > 0
-                    const bool none = c_hi < c_lo;
+                    // an empty interval (or a padded row) becomes c_lo = -1, span = 0:
+                    // every offset is then > 0
+                    const bool none = c_hi < c_lo || qi >= L;
                     const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
                     const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
 #pragma unroll
@@ -723,10 +756,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 r_run = r_run * alpha + ((lr0 + lr1) + (lr2 + lr3));
             }
             if (!ok) break;
-            ok = wait_warp(bar_o, o_use & 1u, abort_flag, limit);
-            ++o_use;
-            if (!ok) break;
-            ptx::tc_fence_after();
+            if (!empty) {
+                ok = wait_warp(bar_o, o_use & 1u, abort_flag, limit);
+                ++o_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
+            }
             // epilogue: O / (sum of rounded P) -> bf16 -> staging block -> TMA store (rows
             // past the sequence end are clipped by the store), and the natural-log LSE
             const float inv_l = r_run > 0.f ? 1.f / r_run : 0.f;
@@ -745,8 +780,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     uint32_t r[32];
-                    ptx::tmem_ld32(t_o + 64 * h + 32 * c2, r);
-                    ptx::tmem_wait_ld();
+                    if (!empty) {
+                        ptx::tmem_ld32(t_o + 64 * h + 32 * c2, r);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = 0u;
+                    }
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint4 val;
@@ -896,7 +936,6 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (causal != 0 && causal != 1) return ATTN_ERR_SHAPE;
-    if (window > 0 && !causal) return ATTN_ERR_UNSUPPORTED;
     // index range: rows fit 32-bit tile arithmetic; unit count fits int
     if (N > (1 << 30)) return ATTN_ERR_SHAPE;
     const long long bh = static_cast<long long>(B) * Hq;
@@ -924,8 +963,9 @@ int encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int
 }
 
 template <int D>
-int launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
-           int N, int causal, int window, float scale, cudaStream_t stream, int sms) {
+int launch(const void *q, const void *k, const void *v, void *o, float *lse, const int *key_len,
+           int B, int Hq, int Hkv, int N, int causal, int window, float scale, cudaStream_t stream,
+           int sms) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
     CUtensorMap mq, mk, mv, mo;
@@ -937,13 +977,16 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     attn::Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
+    p.key_len = key_len;
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.N = N;
     p.group = Hq / Hkv;
     p.causal = causal;
-    p.window = window;
+    // a window of N or more keys excludes nothing: run it as no window (same result)
+    p.window = window >= N ? 0 : window;
+    p.sym = (p.window > 0 && !causal) ? 1 : 0;
     p.n_kv = (N + attn::BN - 1) / attn::BN;
     p.n_pairs = (p.n_kv + 1) / 2;
     p.num_units = B * Hq * p.n_pairs;
@@ -963,15 +1006,29 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
 
 extern "C" {
 
-int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
-             int N, int d, int causal, int window, float scale, void *stream) {
+static int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
+                      const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
+                      int window, float scale, void *stream) {
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
     if (rc != ATTN_OK) return rc;
     int sms = 0;
     if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d == 64) return launch<64>(q, k, v, o, lse, B, Hq, Hkv, N, causal, window, scale, s, sms);
-    return launch<128>(q, k, v, o, lse, B, Hq, Hkv, N, causal, window, scale, s, sms);
+    if (d == 64) return launch<64>(q, k, v, o, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
+    return launch<128>(q, k, v, o, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+             int N, int d, int causal, int window, float scale, void *stream) {
+    return fwd_common(q, k, v, o, lse, nullptr, B, Hq, Hkv, N, d, causal, window, scale, stream);
+}
+
+int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                    float scale, void *stream) {
+    if (!key_len) return ATTN_ERR_NULLPTR;
+    if (misaligned(key_len, 4)) return ATTN_ERR_ALIGN;
+    return fwd_common(q, k, v, o, lse, key_len, B, Hq, Hkv, N, d, causal, window, scale, stream);
 }
 
 int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse, void *dq,

@@ -6,7 +6,10 @@
  *
  *   for every batch b, query head hq, query row i:
  *     kv    = hq / (Hq / Hkv)                               grouped-query head map
- *     J(i)  = { j : (!causal || j <= i) && (window == 0 || i - j < window) }
+ *     L     = N, or key_len[b] for attn_fwd_padded         valid (unpadded) length
+ *     J(i)  = { j : i < L && j < L && (!causal || j <= i)
+ *                   && (window == 0 || i - j < window)
+ *                   && (window == 0 || causal || j - i < window) }
  *     s_ij  = scale * q[b,hq,i,:] . k[b,kv,j,:]              for j in J(i)
  *     lse_i = ln( sum_{j in J(i)} exp(s_ij) )                natural log, scale included
  *     o[b,hq,i,:] = sum_{j in J(i)} exp(s_ij - lse_i) * v[b,kv,j,:]
@@ -22,7 +25,13 @@
  * "방법론"); the tensor layout [batch, heads, n, d] of the framework call
  * F.scaled_dot_product_attention(q, k, v) (devhandbook.co.kr, Example 2). The head
  * map kv = hq / G and the window rule i - j < window are readings of the pages,
- * which name both variants without fixing either.
+ * which name both variants without fixing either; without the look-ahead mask the
+ * window is read symmetrically, |i - j| < window (the sliding-window row of the
+ * devhandbook.co.kr comparison table). Padding follows the guide's padding mask:
+ * padded tokens neither give nor receive attention (section "패딩 마스킹 (Padding
+ * Masking)"), with validity per token read as right padding, as in the
+ * devhandbook.co.kr variable-length example ("Example 7"). A row with no visible key
+ * (a padded row) gets o = 0 and lse = -inf.
  *
  * Conventions shared by every entry point:
  *   - Tensors are dense and contiguous, row-major, in the layouts stated per
@@ -53,8 +62,8 @@ typedef enum {
     ATTN_ERR_ALIGN = -2,       /* q, k, v, o not 16-byte aligned, or lse not 4-byte aligned */
     ATTN_ERR_SHAPE = -3,       /* B, Hq, Hkv or N < 1; Hq % Hkv != 0; window < 0;
                                   scale not finite and > 0; sizes beyond the index range */
-    ATTN_ERR_UNSUPPORTED = -4, /* d not 64 or 128; window > 0 without causal; the current
-                                  device is not an sm_103 (B300-class) GPU */
+    ATTN_ERR_UNSUPPORTED = -4, /* d not 64 or 128; the current device is not an sm_103
+                                  (B300-class) GPU */
     ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed; see attn_last_cuda_error */
     ATTN_ERR_TIMEOUT = -6      /* a kernel wait gave up (reported by attn_device_error) */
 } attn_status;
@@ -71,7 +80,8 @@ typedef enum {
  *        of the scaled scores over J(i))
  *   B, Hq, Hkv, N, d   sizes; Hq must be a multiple of Hkv; d is 64 or 128
  *   causal  0 = bidirectional, 1 = look-ahead mask (j <= i)
- *   window  0 = none; W > 0 (requires causal = 1) restricts keys to i-W+1 .. i
+ *   window  0 = none; W > 0 restricts keys to i-W+1 .. i with causal = 1, and to
+ *           i-W+1 .. i+W-1 without it; W >= N excludes nothing
  *   scale   multiplier of q.k (callers pass 1/sqrt(d)); finite and > 0
  *   stream  cudaStream_t as void*
  *
@@ -80,6 +90,20 @@ typedef enum {
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale,
              void *stream);
+
+/*
+ * attn_fwd_padded -- attn_fwd with per-batch padding.
+ *
+ *   key_len  device, int32 [B], 4-byte aligned (read): the first key_len[b] tokens of
+ *            batch b are valid, the rest are padding (values are clamped to [0, N]).
+ *            Padded keys are invisible to every query; padded query rows see no key
+ *            and get o = 0, lse = -inf.
+ * Every other argument is as for attn_fwd. Query tiles made only of padding load
+ * nothing and write the zero output directly. ATTN_ERR_NULLPTR when key_len is NULL.
+ */
+int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
+                    int window, float scale, void *stream);
 
 /*
  * attn_fwd_host -- the same operation for callers whose tensors live in host memory.

@@ -18,7 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ea.header_functions()
-    assert set(names) >= {"attn_fwd", "attn_fwd_host", "attn_status_str", "attn_last_cuda_error",
+    assert set(names) >= {"attn_fwd", "attn_fwd_padded", "attn_fwd_host", "attn_status_str",
+                          "attn_last_cuda_error",
                           "attn_device_error", "attn_selftest_wait_timeout", "attn_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
@@ -57,7 +58,6 @@ def call(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=1, Hkv=1, N=128, d=64, causal=0
     (dict(causal=2), ea.ATTN_ERR_SHAPE),
     (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
     (dict(d=256), ea.ATTN_ERR_UNSUPPORTED),
-    (dict(window=16, causal=0), ea.ATTN_ERR_UNSUPPORTED),
     (dict(q=A + 8), ea.ATTN_ERR_ALIGN),
     (dict(o=A + 2), ea.ATTN_ERR_ALIGN),
     (dict(lse=A + 2), ea.ATTN_ERR_ALIGN),
@@ -66,6 +66,13 @@ def call(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=1, Hkv=1, N=128, d=64, causal=0
 ])
 def test_rejects_bad_arguments_before_launch(lib, kw, code):
     assert call(lib, **kw) == code
+
+
+def test_padded_entry_validates_key_len(lib):
+    args = [A] * 5
+    assert lib.attn_fwd_padded(*args, None, 1, 1, 1, 128, 64, 0, 0, 0.125, None) == ea.ATTN_ERR_NULLPTR
+    assert lib.attn_fwd_padded(*args, A + 2, 1, 1, 1, 128, 64, 0, 0, 0.125, None) == ea.ATTN_ERR_ALIGN
+    assert lib.attn_fwd_padded(*args, A, 1, 1, 1, 128, 96, 0, 0, 0.125, None) == ea.ATTN_ERR_UNSUPPORTED
 
 
 def test_host_entry_validates_both_buffer_sets(lib):

@@ -181,3 +181,59 @@ def test_bad_arguments_raise():
     with pytest.raises(ea.AttnError) as e:
         ea.attn_fwd(q, q, q)
     assert e.value.code == ea.ATTN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------ symmetric window and padding
+def check_masked(B, Hq, Hkv, N, d, causal, window, seed, key_len=None, scale=None):
+    q, k, v = make_qkv(B, Hq, Hkv, N, d, seed)
+    scale = scale or 1.0 / math.sqrt(d)
+    kl = None if key_len is None else torch.tensor(key_len, dtype=torch.int32, device=DEV)
+    out, lse = ea.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, scale=scale,
+                           key_len=kl)
+    torch.cuda.synchronize()
+    assert ea.device_error() == ea.ATTN_OK
+    o_ref, lse_ref = oracle.attn_ref(q, k, v, causal=causal, window=window, scale=scale, key_len=key_len)
+    dead = ~np.isfinite(lse_ref)           # rows with no visible key (padding)
+    o_g = out.float().cpu().numpy()
+    l_g = lse.cpu().numpy()
+    assert np.all(l_g[dead] == -np.inf) and np.all(o_g[dead] == 0.0), "padded rows must be o=0, lse=-inf"
+    live = ~dead
+    label = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} c{causal} W{window} L{key_len}"
+    return compare(out[torch.from_numpy(live).to(DEV)], lse[torch.from_numpy(live).to(DEV)],
+                   o_ref[live], lse_ref[live], label)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("W", [1, 2, 64, 127, 128, 129, 200, 300, 599, 600, 10000])
+def test_symmetric_window(W, d):
+    check_masked(1, 2, 1, 600, d, False, W, seed=4000 + W)
+
+
+@pytest.mark.parametrize("N,W", [(1, 1), (129, 5), (257, 128), (1000, 256)])
+def test_symmetric_window_lengths(N, W):
+    check_masked(2, 4, 2, N, 128, False, W, seed=4100 + N)
+    check_masked(2, 4, 4, N, 64, False, W, seed=4200 + N)
+
+
+@pytest.mark.parametrize("causal,W", [(False, 0), (True, 0), (True, 100), (False, 100)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_padding(causal, W, d):
+    # lengths: empty, one token, inside a tile, tile edges, full
+    key_len = [0, 1, 77, 128, 129, 255, 256, 300, 513, 700]
+    check_masked(len(key_len), 4, 2, 700, d, causal, W, seed=4300 + d + W, key_len=key_len)
+
+
+def test_padding_full_length_equals_unpadded():
+    q, k, v = make_qkv(2, 4, 4, 333, 64, 44)
+    a = ea.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    kl = torch.full((2,), 333, dtype=torch.int32, device=DEV)
+    b = ea.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, key_len=kl)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_padding_many_units():
+    rng = np.random.default_rng(5)
+    key_len = [int(x) for x in rng.integers(0, 1025, size=24)]
+    check_masked(24, 8, 2, 1024, 128, True, 0, seed=4400, key_len=key_len)
+    check_masked(24, 8, 8, 1024, 64, False, 0, seed=4401, key_len=key_len)
