@@ -11,6 +11,8 @@ rows); this module only compiles it with gcc and marshals numpy arrays.
 Parity status of each function (see the pins in ``tests/test_oracle_pins.py``):
   attn_ref / attn_ref_rows -- pinned (closed forms, invariants, brute force,
   an independent library routine, and mutation tests).
+  attn_ref_decode -- pinned (the last rows of the plain forward, a zero-query closed
+  form, brute force and torch SDPA with an offset mask).
 """
 from __future__ import annotations
 
@@ -53,6 +55,10 @@ def _declare(lib):
         u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
         i32p, f64p, f64p, ctypes.c_int]
     lib.attn_ref_fwd_f64.restype = ctypes.c_int
+    lib.attn_ref_decode_rows_f64.argtypes = [
+        u16p, u16p, u16p, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
+        i64p, i64, f64p, f64p, ctypes.c_int]
+    lib.attn_ref_decode_rows_f64.restype = ctypes.c_int
     return lib
 
 
@@ -137,3 +143,34 @@ def attn_ref(q, k, v, causal: bool = False, window: int = 0, scale: float | None
         scale = 1.0 / float(np.sqrt(d))
     o, lse = attn_ref_rows(qb, k, v, causal, window, scale, None, nthreads, lib, key_len)
     return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)
+
+
+def attn_ref_decode(q, k, v, causal: bool = True, window: int = 0, scale: float | None = None,
+                    rows=None, nthreads: int | None = None, lib=None):
+    """Decode shape: q [B,Hq,Nq,d] are the last Nq positions of a sequence whose keys
+    and values k, v are [B,Hkv,Nk,d]. Returns fp64 (o, lse) shaped [B,Hq,Nq,d] and
+    [B,Hq,Nq], or [nrows,d] and [nrows] for a list of flat rows ((b*Hq)+hq)*Nq + i."""
+    qb, kb, vb = _as_bits(q), _as_bits(k), _as_bits(v)
+    B, Hq, Nq, d = qb.shape
+    Hkv, Nk = kb.shape[1], kb.shape[2]
+    if kb.shape != (B, Hkv, Nk, d) or vb.shape != kb.shape:
+        raise ValueError("k and v must be [B,Hkv,Nk,d] matching q")
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    rows_arr = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = B * Hq * Nq if rows_arr is None else rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    L = lib or load()
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = L.attn_ref_decode_rows_f64(
+        qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p),
+        B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), int(window), float(scale),
+        rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
+        nrows, o.ctypes.data_as(f64p), lse.ctypes.data_as(f64p), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    if rows_arr is None:
+        return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
+    return o, lse

@@ -42,6 +42,12 @@
  *     "Example 7"), read as right padding: batch b's first key_len[b] tokens are
  *     valid. A padded query row therefore has no visible key.
  *
+ * Decode shape (attn_ref_decode_rows_f64): Nq query rows against Nk >= Nq keys, the
+ * queries being the last Nq positions of the sequence: query row i stands at position
+ * i + Nk - Nq, and the mask above applies to that position (a key-value cache read by
+ * the newest tokens, the generation stage of the SpAtten review's "Background"
+ * section). With Nq = Nk this is the plain forward.
+ *
  * Inputs are bf16 bit patterns (uint16); each is widened exactly to fp64.
  * A row whose visible set is empty (impossible for valid arguments, since j = i is
  * always visible) yields o = 0 and lse = -inf.
@@ -69,7 +75,8 @@ static int key_visible(int64_t i, int64_t j, int causal, int64_t window, int64_t
 
 typedef struct {
     const uint16_t *q, *k, *v;
-    int64_t B, Hq, Hkv, N, d;
+    int64_t B, Hq, Hkv, N, d;   /* N: query rows per head */
+    int64_t Nk;                 /* keys per head; query row i stands at i + Nk - N */
     int causal;
     int64_t window;
     double scale;
@@ -82,28 +89,29 @@ typedef struct {
 /* One query row, straight from the definition above. */
 static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_out,
                     double *qd, double *s) {
-    const int64_t N = jb->N, d = jb->d;
+    const int64_t N = jb->N, d = jb->d, Nk = jb->Nk;
     const int64_t i = flat % N;
     const int64_t bh = flat / N;
     const int64_t hq = bh % jb->Hq;
     const int64_t b = bh / jb->Hq;
     const int64_t group = jb->Hq / jb->Hkv;
     const int64_t kv = hq / group;
-    int64_t L = jb->key_len ? (int64_t)jb->key_len[b] : N;
+    int64_t L = jb->key_len ? (int64_t)jb->key_len[b] : Nk;
     if (L < 0) L = 0;
-    if (L > N) L = N;
+    if (L > Nk) L = Nk;
+    const int64_t pos = i + (Nk - N);   /* position of query row i in the sequence */
 
     const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;
-    const uint16_t *kbase = jb->k + (b * jb->Hkv + kv) * N * d;
-    const uint16_t *vbase = jb->v + (b * jb->Hkv + kv) * N * d;
+    const uint16_t *kbase = jb->k + (b * jb->Hkv + kv) * Nk * d;
+    const uint16_t *vbase = jb->v + (b * jb->Hkv + kv) * Nk * d;
 
     for (int64_t c = 0; c < d; ++c) qd[c] = bf16_bits_to_double(qrow[c]);
 
     /* scores over the visible keys */
     double m = -INFINITY;
     int64_t nvis = 0;
-    for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (!key_visible(pos, j, jb->causal, jb->window, L)) continue;
         const uint16_t *krow = kbase + j * d;
         double dot = 0.0;
         for (int64_t c = 0; c < d; ++c) dot += qd[c] * bf16_bits_to_double(krow[c]);
@@ -119,16 +127,16 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
 
     /* log-sum-exp */
     double l = 0.0;
-    for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (!key_visible(pos, j, jb->causal, jb->window, L)) continue;
         l += exp(s[j] - m);
     }
     const double lse = m + log(l);
     *lse_out = lse;
 
     /* probability-weighted sum of value rows */
-    for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (!key_visible(pos, j, jb->causal, jb->window, L)) continue;
         const double p = exp(s[j] - lse);
         const uint16_t *vrow = vbase + j * d;
         for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_bits_to_double(vrow[c]);
@@ -138,7 +146,7 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
 static void *worker(void *arg) {
     const job_t *jb = (const job_t *)arg;
     double *qd = (double *)malloc(sizeof(double) * (size_t)jb->d);
-    double *s = (double *)malloc(sizeof(double) * (size_t)jb->N);
+    double *s = (double *)malloc(sizeof(double) * (size_t)jb->Nk);
     if (qd && s) {
         for (int64_t r = jb->row_begin; r < jb->row_end; ++r) {
             const int64_t flat = jb->rows ? jb->rows[r] : r;
@@ -165,14 +173,14 @@ static int check_args(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
  * o: nrows * d doubles, lse: nrows doubles. Returns 0, or a negative code for bad
  * arguments (-1 null pointer, -3 shape, -4 unsupported combination).
  */
-int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                          int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
-                          int causal, int64_t window, double scale, const int32_t *key_len,
-                          const int64_t *rows, int64_t nrows, double *o, double *lse,
-                          int nthreads) {
+static int rows_core(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t Nk, int64_t d,
+                     int causal, int64_t window, double scale, const int32_t *key_len,
+                     const int64_t *rows, int64_t nrows, double *o, double *lse, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
     int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
     if (rc) return rc;
+    if (Nk < N) return -3;
     if (nrows < 0) return -3;
     if (!rows && nrows != B * Hq * N) return -3;
     if (rows) {
@@ -193,7 +201,7 @@ int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *
     for (int t = 0; t < nthreads; ++t) {
         job_t *jb = &jobs[t];
         jb->q = q; jb->k = k; jb->v = v;
-        jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d;
+        jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d; jb->Nk = Nk;
         jb->causal = causal; jb->window = window; jb->scale = scale;
         jb->key_len = key_len;
         jb->rows = rows;
@@ -213,6 +221,28 @@ int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *
     free(jobs);
     free(tids);
     return 0;
+}
+
+/* Plain forward (Nq = Nk = N): the rows listed in `rows` (flat ids ((b*Hq)+hq)*N + i),
+ * or all rows in order when rows is NULL. key_len may be NULL. */
+int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                          int causal, int64_t window, double scale, const int32_t *key_len,
+                          const int64_t *rows, int64_t nrows, double *o, double *lse,
+                          int nthreads) {
+    return rows_core(q, k, v, B, Hq, Hkv, N, N, d, causal, window, scale, key_len, rows, nrows,
+                     o, lse, nthreads);
+}
+
+/* Decode shape: q [B,Hq,Nq,d], k and v [B,Hkv,Nk,d], Nk >= Nq; rows are flat ids
+ * ((b*Hq)+hq)*Nq + i, or all rows when NULL; o [nrows,d], lse [nrows]. */
+int attn_ref_decode_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
+                             int causal, int64_t window, double scale,
+                             const int64_t *rows, int64_t nrows, double *o, double *lse,
+                             int nthreads) {
+    return rows_core(q, k, v, B, Hq, Hkv, Nq, Nk, d, causal, window, scale, NULL, rows, nrows,
+                     o, lse, nthreads);
 }
 
 /* All rows: o is [B,Hq,N,d], lse is [B,Hq,N], both fp64. key_len may be NULL. */

@@ -21,6 +21,8 @@ What pins what:
                     see nothing); valid rows equal the batch truncated to its length
   symmetric window  one-hot closed form for |i - j| < W; W >= N equals bidirectional;
                     brute force and torch SDPA with padding and both window kinds
+  decode shape      queries at the end of a sequence equal the plain forward's last
+                    rows; zero-query closed form; brute force and torch SDPA
 """
 from __future__ import annotations
 
@@ -430,7 +432,74 @@ def pin_masks_torch_sdpa(lib):
             _close(o[b, :, :L], ref[0, :, :L].numpy(), 1e-12, f"torch SDPA masks b={b} c={causal} W={W}")
 
 
+# ---------------------------------------------------------------- decode shape
+def pin_decode_equals_last_rows(lib):
+    # Nq queries at the end of an Nk-token sequence are the last Nq rows of the plain
+    # forward over all Nk tokens
+    g = torch.Generator().manual_seed(31)
+    B, Hq, Hkv, Nk, d = 2, 4, 2, 37, 16
+    q = torch.randn(B, Hq, Nk, d, generator=g).bfloat16()
+    k = torch.randn(B, Hkv, Nk, d, generator=g).bfloat16()
+    v = torch.randn(B, Hkv, Nk, d, generator=g).bfloat16()
+    for causal, W in [(True, 0), (True, 5), (False, 0), (False, 7)]:
+        of, lf = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=0.3, lib=lib)
+        for Nq in (1, 3, 37):
+            od, ld = oracle.attn_ref_decode(q[:, :, Nk - Nq:].contiguous(), k, v, causal=causal,
+                                            window=W, scale=0.3, lib=lib)
+            assert np.array_equal(od, of[:, :, Nk - Nq:]) and np.array_equal(ld, lf[:, :, Nk - Nq:]), \
+                f"decode != last rows (causal={causal} W={W} Nq={Nq})"
+
+
+def pin_decode_zero_query(lib):
+    g = torch.Generator().manual_seed(32)
+    B, Nq, Nk, d = 1, 3, 20, 8
+    q = torch.zeros(B, 2, Nq, d, dtype=torch.bfloat16)
+    k = torch.randn(B, 1, Nk, d, generator=g).bfloat16()
+    v = torch.randn(B, 1, Nk, d, generator=g).bfloat16()
+    vd = f64(v)
+    for causal, W in [(True, 0), (True, 4), (False, 0)]:
+        o, lse = oracle.attn_ref_decode(q, k, v, causal=causal, window=W, scale=0.5, lib=lib)
+        for i in range(Nq):
+            pos = Nk - Nq + i
+            js = [j for j in range(Nk) if _visible(pos, j, causal, W, Nk)]
+            for h in range(2):
+                _close(lse[0, h, i], math.log(len(js)), 1e-13, "decode zero-q lse")
+                _close(o[0, h, i], vd[0, 0, js].mean(axis=0), 1e-13, "decode zero-q O")
+
+
+def pin_decode_brute_force_and_sdpa(lib):
+    import mpmath
+    import torch.nn.functional as F
+    mpmath.mp.dps = 40
+    g = torch.Generator().manual_seed(33)
+    B, Hq, Hkv, Nq, Nk, d = 1, 4, 1, 2, 13, 4
+    q = (2 * torch.randn(B, Hq, Nq, d, generator=g)).bfloat16()
+    k = (2 * torch.randn(B, Hkv, Nk, d, generator=g)).bfloat16()
+    v = torch.randn(B, Hkv, Nk, d, generator=g).bfloat16()
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    for causal, W in [(True, 0), (True, 6)]:
+        o, lse = oracle.attn_ref_decode(q, k, v, causal=causal, window=W, scale=0.5, lib=lib)
+        for h in range(Hq):
+            for i in range(Nq):
+                pos = Nk - Nq + i
+                js = [j for j in range(Nk) if _visible(pos, j, causal, W, Nk)]
+                s = {j: mpmath.mpf(0.5) * mpmath.fsum(mpmath.mpf(qd[0, h, i, c]) * mpmath.mpf(kd[0, 0, j, c])
+                                                     for c in range(d)) for j in js}
+                z = mpmath.fsum(mpmath.exp(s[j]) for j in js)
+                _close(lse[0, h, i], float(mpmath.log(z)), 1e-13, "decode brute-force lse")
+                ob = [float(mpmath.fsum(mpmath.exp(s[j]) * mpmath.mpf(vd[0, 0, j, c]) for j in js) / z)
+                      for c in range(d)]
+                _close(o[0, h, i], ob, 1e-13, "decode brute-force O")
+        i = torch.arange(Nq).view(Nq, 1) + (Nk - Nq)
+        j = torch.arange(Nk).view(1, Nk)
+        mask = (j <= i) & ((i - j) < W if W else torch.ones(Nq, Nk, dtype=torch.bool))
+        ref = F.scaled_dot_product_attention(q.double(), k.double().repeat_interleave(Hq, 1),
+                                             v.double().repeat_interleave(Hq, 1), attn_mask=mask, scale=0.5)
+        _close(o, ref.numpy(), 1e-12, "decode torch SDPA")
+
+
 ALL_PINS = [pin_worked_example, pin_one_hot, pin_zero_query, pin_constant_v, pin_causal_row0,
             pin_gqa, pin_window_ge_n, pin_permutation, pin_brute_force, pin_torch_sdpa,
             pin_padding_zero_query, pin_padding_truncation, pin_symmetric_window_one_hot,
-            pin_symmetric_window_ge_n, pin_masks_brute_force, pin_masks_torch_sdpa]
+            pin_symmetric_window_ge_n, pin_masks_brute_force, pin_masks_torch_sdpa,
+            pin_decode_equals_last_rows, pin_decode_zero_query, pin_decode_brute_force_and_sdpa]

@@ -38,6 +38,8 @@ MUTANTS = {
     # the symmetric window's right edge is off by one
     "symmetric_window_off_by_one": ("if (window > 0 && !causal && j - i >= window) return 0;",
                                     "if (window > 0 && !causal && j - i > window) return 0;"),
+    # decode queries placed at the start of the sequence instead of its end
+    "decode_offset_missing": ("const int64_t pos = i + (Nk - N);", "const int64_t pos = i;"),
     # value accumulation misses the probability weight normalisation
     "unnormalised_output": ("const double p = exp(s[j] - lse);", "const double p = exp(s[j] - m);"),
 }
