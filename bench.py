@@ -36,7 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from exact_self_attention_fwd_b300.inputs import WORKLOADS, Workload, make_qkv  # noqa: E402
+from exact_self_attention_fwd_b300.inputs import (DECODE_WORKLOADS, WORKLOADS, DecodeWorkload,  # noqa: E402
+                                                   Workload, make_qkv, make_qkv_decode)
 
 DEFAULT_WORKLOAD = "gqa_8k"
 FLUSH_BYTES = 256 << 20
@@ -66,6 +67,21 @@ def hbm_bytes(w: Workload) -> int:
     q = w.B * w.Hq * w.N * w.d * 2
     kv = 2 * w.B * w.Hkv * w.N * w.d * 2
     return q + kv + q + w.B * w.Hq * w.N * 4
+
+
+def decode_flops(w: DecodeWorkload) -> int:
+    """4 d per visible (query, key) pair; query i stands at position i + Nk - Nq."""
+    pairs = 0
+    for i in range(w.Nq):
+        pos = i + w.Nk - w.Nq
+        pairs += (pos + 1) if w.causal else w.Nk
+    return 4 * w.B * w.Hq * pairs * w.d
+
+
+def decode_hbm_bytes(w: DecodeWorkload) -> int:
+    """Q, K, V read once (bf16), O written (bf16), LSE written (fp32)."""
+    q = w.B * w.Hq * w.Nq * w.d * 2
+    return 2 * q + 2 * w.B * w.Hkv * w.Nk * w.d * 2 + w.B * w.Hq * w.Nq * 4
 
 
 def kernel_sha() -> str:
@@ -373,6 +389,39 @@ def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset:
     return per, "per-call CUDA events, L2 flushed between calls"
 
 
+def measure_decode(ea, w: DecodeWorkload, dev, steps: int, warmup: int, seed_offset: int = 0):
+    """Device time per attn_fwd_decode call (seconds), per-call CUDA events, L2 flushed
+    between calls; the split workspace is allocated once, outside the timed calls."""
+    import torch
+    q, k, v = make_qkv_decode(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.seed + seed_offset)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+    need = ea.decode_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, 0)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        ea.attn_fwd_decode(qd, kd, vd, causal=w.causal, scale=w.scale, out=out, lse=lse, workspace=ws,
+                           stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
+
+
 def run_ours(args, w: Workload):
     import torch
 
@@ -478,6 +527,15 @@ def run_ours(args, w: Workload):
             summary[name] = {"tflops": flops(ww) / t_call / 1e12, "us_per_call": t_call * 1e6,
                              "gbs": hbm_bytes(ww) / t_call / 1e9, "bound": r["bound"],
                              "frac": r["frac"], "timing": how}
+        for name, dw in DECODE_WORKLOADS.items():
+            t_call = measure_decode(ea, dw, dev, args.summary_steps, 5, seed_offset=rank)
+            gbs = decode_hbm_bytes(dw) / t_call / 1e9
+            summary[name] = {"tflops": decode_flops(dw) / t_call / 1e12, "us_per_call": t_call * 1e6,
+                             "gbs": gbs, "bound": "hbm",
+                             "frac": gbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                             "timing": "per-call CUDA events, L2 flushed between calls",
+                             "entry": "attn_fwd_decode (split key sequence + merge kernel)",
+                             "shape": dw.note}
 
     if rank == 0:
         peaks, peak_src = load_peaks()

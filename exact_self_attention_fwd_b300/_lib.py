@@ -22,6 +22,7 @@ ATTN_ERR_SHAPE = -3
 ATTN_ERR_UNSUPPORTED = -4
 ATTN_ERR_CUDA = -5
 ATTN_ERR_TIMEOUT = -6
+ATTN_ERR_WORKSPACE = -7
 
 _lib = None
 
@@ -46,6 +47,11 @@ def _declare(lib):
     lib.attn_fwd.restype = i
     lib.attn_fwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_padded.restype = i
+    lib.attn_fwd_decode_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.attn_fwd_decode_workspace_size.restype = ctypes.c_size_t
+    lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
+                                    ctypes.c_size_t, vp]
+    lib.attn_fwd_decode.restype = i
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_host.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -147,6 +153,50 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
                                    lse.data_ptr(), key_len.data_ptr(), B, Hq, Hkv, N, d,
                                    int(bool(causal)), int(window), float(scale),
                                    _stream_handle(stream, dev))
+    _check(rc)
+    return out, lse
+
+
+def decode_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, splits: int = 0) -> int:
+    """Bytes of workspace attn_fwd_decode needs (0 when it runs unsplit)."""
+    return int(load().attn_fwd_decode_workspace_size(B, Hq, Hkv, Nq, Nk, d, int(splits)))
+
+
+def attn_fwd_decode(q, k, v, causal: bool = True, window: int = 0, scale: float | None = None,
+                    splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """Decode shape: CUDA bf16 q [B,Hq,Nq,d] are the last Nq positions of a sequence whose
+    keys and values are k, v [B,Hkv,Nk,d]. Returns (o [B,Hq,Nq,d] bf16, lse [B,Hq,Nq] fp32).
+
+    splits: parts of the key sequence computed by separate CTAs (0 = the library's
+    choice). The fp32 workspace for the partial results is allocated here with torch
+    when not given (uint8 CUDA tensor of at least decode_workspace_size(...) bytes)."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    dev = q.device
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    L = load()
+    with torch.cuda.device(dev):
+        need = int(L.attn_fwd_decode_workspace_size(B, Hq, Hkv, Nq, Nk, d, int(splits)))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = L.attn_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), int(window), float(scale),
+                               int(splits), ws_ptr, ws_bytes, _stream_handle(stream, dev))
     _check(rc)
     return out, lse
 

@@ -104,6 +104,14 @@ struct Params {
     float sl2;  // scale * log2(e)
     unsigned long long timeout_ns;
     FastDiv div_bh, div_hq, div_group;  // by B * Hq, Hq and Hq / Hkv
+    // key-side length and query offset: keys per head Nk (= N except in the decode
+    // shape), and query row i stands at position i + pos_off
+    int Nk, pos_off;
+    // decode shape: query tiles pack the G * Nq rows of one KV head (N = G * Nq rows
+    // per tensor-map z index); unit = (batch * Hkv + hkv, split of the key tiles)
+    int Nq, splits, split_lo, split_len, split_hi;
+    FastDiv div_splits, div_nq;
+    float *o_part, *lse_part;  // partial results per split (splits > 1), fp32
 };
 
 template <int D>
@@ -271,17 +279,60 @@ __device__ __forceinline__ void tile_range(const Params &p, int q0, int L, int &
 
 // a (query tile, key tile) block needs element masking when it crosses the end of
 // the sequence, the causal diagonal or the window edge
-__device__ __forceinline__ bool block_needs_mask(const Params &p, int q0, int kv0, int L) {
-    if (kv0 + BN > L) return true;                                     // keys past the valid end
-    if (L < p.N && q0 + BM > L) return true;                           // padded query rows
-    if (p.causal && kv0 + BN - 1 > q0) return true;                    // the diagonal
-    if (p.window > 0 && (q0 + BM - 1) - kv0 >= p.window) return true;  // the window's lower edge
-    if (p.sym && kv0 + BN - 1 > q0 + p.window - 1) return true;        // the upper edge
+// (rows at positions pos_first .. pos_last; padded: some rows are padding)
+__device__ __forceinline__ bool block_needs_mask(const Params &p, int pos_first, int pos_last,
+                                                 int kv0, int L, bool padded) {
+    if (kv0 + BN > L) return true;                                      // keys past the valid end
+    if (padded) return true;                                            // padded query rows
+    if (p.causal && kv0 + BN - 1 > pos_first) return true;              // the diagonal
+    if (p.window > 0 && pos_last - kv0 >= p.window) return true;        // the window's lower edge
+    if (p.sym && kv0 + BN - 1 > pos_first + p.window - 1) return true;  // the upper edge
     return false;
 }
 
+// query/output rows of one split in the decode shape: rows per z index x z indices
+__device__ __forceinline__ size_t rows_per_split(const Params &p) {
+    return static_cast<size_t>(p.N) * static_cast<size_t>(p.B) * static_cast<size_t>(p.Hkv);
+}
+
+// What a work unit covers: the tensor-map z index of its query/output rows and of its
+// keys/values, the first row of its first query tile (the second starts BM rows
+// later), the key tiles [lo_t, hi_t) each query tile visits, and the valid key length.
+struct UnitInfo {
+    int zq, zkv, q0a, L, split;
+    int lo0, hi0, lo1, hi1;
+};
+
+template <bool DEC>
+__device__ __forceinline__ UnitInfo unit_info(int u, const Params &p) {
+    UnitInfo ui;
+    if constexpr (!DEC) {
+        const Unit w = decode_unit(u, p);
+        ui.zq = w.b * p.Hq + w.hq;
+        ui.zkv = w.b * p.Hkv + w.hkv;
+        ui.q0a = 2 * w.pair * BM;
+        ui.L = valid_len(p, w.b);
+        ui.split = 0;
+        tile_range(p, ui.q0a, ui.L, ui.lo0, ui.hi0);
+        tile_range(p, ui.q0a + BM, ui.L, ui.lo1, ui.hi1);
+    } else {
+        // one query tile holding the G * Nq rows that read KV head zkv; the split takes
+        // a contiguous share of the key tiles the rows can see
+        const int bhkv = fdiv(u, p.div_splits);
+        ui.split = u - bhkv * p.splits;
+        ui.zq = ui.zkv = bhkv;
+        ui.q0a = 0;
+        ui.L = p.Nk;
+        ui.lo0 = p.split_lo + ui.split * p.split_len;
+        ui.hi0 = min(ui.lo0 + p.split_len, p.split_hi);
+        if (ui.hi0 <= ui.lo0) ui.lo0 = ui.hi0 = 0;  // nothing left for this split
+        ui.lo1 = ui.hi1 = 0;
+    }
+    return ui;
+}
+
 // ------------------------------------------------------------------ kernel
-template <int D>
+template <int D, bool DEC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -349,20 +400,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t kv_it = 0, q_it = 0;
             bool ok = true;
             for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
-                const Unit w = decode_unit(u, p);
-                const int q0a = 2 * w.pair * BM, q0b = q0a + BM;
-                int lo0, hi0, lo1, hi1;
-                const int L = valid_len(p, w.b);
-                tile_range(p, q0a, L, lo0, hi0);
-                tile_range(p, q0b, L, lo1, hi1);
-                // a first tile without visible keys has only padded rows, and so has the
-                // second: nothing to load (the softmax warps write the zero output)
+                const UnitInfo ui = unit_info<DEC>(u, p);
+                const int q0a = ui.q0a, q0b = q0a + BM;
+                const int lo0 = ui.lo0, hi0 = ui.hi0, lo1 = ui.lo1, hi1 = ui.hi1;
+                // a first tile without visible keys has only padded rows (or an empty
+                // split), and so has the second: nothing to load (the softmax warps write
+                // the zero output)
                 if (hi0 <= lo0) continue;
                 const bool has1 = hi1 > lo1;
                 const int lo = has1 ? min(lo0, lo1) : lo0;
                 const int hi = has1 ? max(hi0, hi1) : hi0;
-                const int zq = w.b * p.Hq + w.hq;
-                const int zkv = w.b * p.Hkv + w.hkv;
+                const int zq = ui.zq;
+                const int zkv = ui.zkv;
                 // Q buffer of this unit; its previous contents (the unit Q_BUFS units
                 // back) are free once that unit's last S product has completed
                 const uint32_t qb = q_it % C::Q_BUFS, qph = (q_it / C::Q_BUFS) & 1u;
@@ -463,13 +512,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
 
             for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
-                const Unit w = decode_unit(u, p);
-                const int q0a = 2 * w.pair * BM;
-                int lo0, hi0, lo1, hi1;
-                const int L = valid_len(p, w.b);
-                tile_range(p, q0a, L, lo0, hi0);
-                tile_range(p, q0a + BM, L, lo1, hi1);
-                if (hi0 <= lo0) continue;  // padding only: nothing to compute
+                const UnitInfo ui = unit_info<DEC>(u, p);
+                const int lo0 = ui.lo0, hi0 = ui.hi0, lo1 = ui.lo1, hi1 = ui.hi1;
+                if (hi0 <= lo0) continue;  // padding only (or an empty split): nothing to compute
                 const bool has1 = hi1 > lo1;
                 const int lo = has1 ? min(lo0, lo1) : lo0;
                 const int hi = has1 ? max(hi0, hi1) : hi0;
@@ -616,6 +661,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool store_thread = (quad == 0 && lane == 0);  // issues this warpgroup's O stores
         const uint32_t bar_efree = bar(C::B_EFREE + t), bar_efull = bar(C::B_EFULL + t);
         uint32_t e_use = 0;
+        // decode shape: tile row r holds query r % Nq (of head r / Nq of the group)
+        int my_dec_pos = 0;
+        if constexpr (DEC) my_dec_pos = p.pos_off + (row - fdiv(row, p.div_nq) * p.Nq);
         const uint32_t bar_s = bar(C::B_SFULL + t), bar_o = bar(C::B_OFULL + t);
         const uint32_t bar_sfree = bar(C::B_SFREE + t), bar_pvdone = bar(C::B_PVDONE + t);
         uint32_t pv_w = 0;
@@ -624,14 +672,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t s_use = 0, o_use = 0;
         bool ok = true;
         for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
-            const Unit w = decode_unit(u, p);
-            const int q0 = (2 * w.pair + t) * BM;
-            int lo, hi;
+            const UnitInfo ui = unit_info<DEC>(u, p);
+            const int q0 = ui.q0a + t * BM;
             if (q0 >= p.N) continue;  // no rows in this tile
-            const int L = valid_len(p, w.b);
-            tile_range(p, q0, L, lo, hi);
-            const bool empty = hi <= lo;  // all rows padded: the output is zero
+            const int lo = t ? ui.lo1 : ui.lo0, hi = t ? ui.hi1 : ui.hi0;
+            const int L = ui.L;
+            const bool empty = hi <= lo;  // all rows padded (or an empty split): zero output
             const int qi = q0 + row;
+            // this row's position in the sequence, and whether it is a real query row
+            const int pos = DEC ? my_dec_pos : qi;
+            const bool row_live = DEC ? true : (qi < L);
+            // positions of the tile's first and last rows, for the edge-tile test
+            const int pos_first = DEC ? p.pos_off : q0;
+            const int pos_last = DEC ? p.Nk - 1 : q0 + BM - 1;
+            const bool padded_rows = DEC ? false : (L < p.N && q0 + BM > L);
             float m_run = -INFINITY;  // running max of scale*s*log2(e)
             float l_run = 0.f;        // running sum of 2^(x - m_run), for the LSE
             float r_run = 0.f;        // running sum of bf16(2^(x - m_run)), for normalising O
@@ -651,20 +705,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) ptx::mbar_arrive(bar_sfree);
                 }
                 const int kv0 = j * BN;
-                if (block_needs_mask(p, q0, kv0, L)) {
+                if (block_needs_mask(p, pos_first, pos_last, kv0, L, padded_rows)) {
                     // The keys row qi sees in this tile form one interval of columns
                     // [c_lo, c_hi]: c_hi from the sequence end and the causal diagonal,
                     // c_lo from the window. One unsigned compare per element against the
                     // column index (a compile-time constant) keeps this rarely run block
                     // small.
                     int c_hi = L - 1;
-                    if (p.causal) c_hi = min(c_hi, qi);
-                    if (p.sym) c_hi = min(c_hi, qi + p.window - 1);
+                    if (p.causal) c_hi = min(c_hi, pos);
+                    if (p.sym) c_hi = min(c_hi, pos + p.window - 1);
                     c_hi -= kv0;
-                    const int c_lo = p.window > 0 ? max(qi - p.window + 1 - kv0, 0) : 0;
+                    const int c_lo = p.window > 0 ? max(pos - p.window + 1 - kv0, 0) : 0;
                     // an empty interval (or a padded row) becomes c_lo = -1, span = 0:
                     // every offset is then > 0
-                    const bool none = c_hi < c_lo || qi >= L;
+                    const bool none = c_hi < c_lo || !row_live;
                     const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
                     const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
 #pragma unroll
@@ -765,9 +819,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // epilogue: O / (sum of rounded P) -> bf16 -> staging block -> TMA store (rows
             // past the sequence end are clipped by the store), and the natural-log LSE
             const float inv_l = r_run > 0.f ? 1.f / r_run : 0.f;
-            const size_t ridx = static_cast<size_t>(w.b * p.Hq + w.hq) * static_cast<size_t>(p.N) +
+            const size_t ridx = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
-            const int zq = w.b * p.Hq + w.hq;
+            const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            const int zq = ui.zq;
+            if constexpr (DEC) {
+                if (p.splits > 1) {
+                    // split of the key sequence: this unit's normalised O (fp32) and LSE go
+                    // to the partial buffers, which the combine kernel merges. The
+                    // tensor-memory loads are warp-collective: every lane takes them, and
+                    // only rows of the packed tile store.
+                    const bool store_row = qi < p.N;
+                    const size_t prow = static_cast<size_t>(ui.split) * rows_per_split(p) + ridx;
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D);
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        if (!empty) {
+                            ptx::tmem_ld32(t_o + 32 * c, r);
+                            ptx::tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) r[e] = 0u;
+                        }
+                        if (store_row) {
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                dst[c * 8 + g] = make_float4(__uint_as_float(r[4 * g + 0]) * inv_l,
+                                                             __uint_as_float(r[4 * g + 1]) * inv_l,
+                                                             __uint_as_float(r[4 * g + 2]) * inv_l,
+                                                             __uint_as_float(r[4 * g + 3]) * inv_l);
+                        }
+                    }
+                    if (store_row) p.lse_part[prow] = lse_nat;
+                    continue;
+                }
+            }
 #pragma unroll 1
             for (int h = 0; ok && h < D / 64; ++h) {
                 // the staging block is free once the previous store from it has read it
@@ -816,7 +903,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++e_use;
             }
             if (!ok) break;
-            if (qi < p.N) p.lse[ridx] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            if (qi < p.N) p.lse[ridx] = lse_nat;
         }
         // the O stores read shared memory and write global memory after they are issued:
         // both must be done before the CTA exits
@@ -829,6 +916,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// Decode shape, split key sequence: merge the per-split results of each packed query
+// row. With lse_s and o_s (o_s normalised within split s), lse = ln sum_s exp(lse_s)
+// and o = sum_s exp(lse_s - lse) o_s: the log-sum-exp merge of partial softmaxes
+// (splits with no visible key carry lse_s = -inf and weigh nothing). One warp per row,
+// each lane owning D / 32 consecutive columns.
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float *__restrict__ o_part,
+                                                             const float *__restrict__ lse_part,
+                                                             __nv_bfloat16 *__restrict__ o,
+                                                             float *__restrict__ lse, int rows,
+                                                             int splits) {
+    constexpr int PER = D / 32;
+    const int row = blockIdx.x * 8 + static_cast<int>(threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float m = -INFINITY;
+    for (int s = lane; s < splits; s += 32) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float sum = 0.f;
+    if (m != -INFINITY) {
+        for (int s = lane; s < splits; s += 32) {
+            const float l = lse_part[static_cast<size_t>(s) * rows + row];
+            if (l != -INFINITY) sum += expf(l - m);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float lse_row = (m == -INFINITY) ? -INFINITY : m + logf(sum);
+    float acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+    if (m != -INFINITY) {
+        for (int s = 0; s < splits; ++s) {
+            const float l = lse_part[static_cast<size_t>(s) * rows + row];
+            if (l == -INFINITY) continue;
+            const float wgt = expf(l - lse_row);
+            const float *src = o_part + (static_cast<size_t>(s) * rows + row) * D + lane * PER;
+            if constexpr (PER == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(wgt, x.x, acc[0]);
+                acc[1] = fmaf(wgt, x.y, acc[1]);
+                acc[2] = fmaf(wgt, x.z, acc[2]);
+                acc[3] = fmaf(wgt, x.w, acc[3]);
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(wgt, x.x, acc[0]);
+                acc[1] = fmaf(wgt, x.y, acc[1]);
+            }
+        }
+    }
+    uint32_t *dst = reinterpret_cast<uint32_t *>(o + static_cast<size_t>(row) * D + lane * PER);
+#pragma unroll
+    for (int c = 0; c < PER / 2; ++c) dst[c] = ptx::pack_bf16x2(acc[2 * c], acc[2 * c + 1]);
+    if (lane == 0) lse[row] = lse_row;
 }
 
 // One warp waits on a barrier nothing will complete; exercises the timeout path.
@@ -903,8 +1047,10 @@ int device_setup(int *sms_out) {
         if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
         // the warpgroup register split must fit in what a CTA is launched with;
         // otherwise setmaxnreg.inc would wait for registers that never come
-        const void *kernels[2] = {reinterpret_cast<const void *>(attn::attn_fwd_kernel<64>),
-                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128>)};
+        const void *kernels[4] = {reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, true>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, true>)};
         for (const void *kfn : kernels) {
             cudaFuncAttributes fa;
             if ((e = cudaFuncGetAttributes(&fa, kfn)) != cudaSuccess) return cuda_fail(e);
@@ -912,10 +1058,16 @@ int device_setup(int *sms_out) {
                 2 * 128 * attn::SOFTMAX_REGS + 128 * attn::PRODUCER_REGS)
                 return ATTN_ERR_UNSUPPORTED;
         }
-        if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
+        if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<128>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<128>::SMEM_ALLOC)) != cudaSuccess)
             return cuda_fail(e);
@@ -995,10 +1147,136 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, con
     p.div_bh = attn::make_fastdiv(static_cast<uint32_t>(B * Hq));
     p.div_hq = attn::make_fastdiv(static_cast<uint32_t>(Hq));
     p.div_group = attn::make_fastdiv(static_cast<uint32_t>(p.group));
+    p.Nk = N;
+    p.pos_off = 0;
+    p.Nq = N;
+    p.splits = 1;
+    p.split_lo = p.split_len = p.split_hi = 0;
+    p.div_splits = attn::make_fastdiv(1u);
+    p.div_nq = attn::make_fastdiv(1u);
+    p.o_part = p.lse_part = nullptr;
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    attn::attn_fwd_kernel<D, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+// Split count for the decode shape: units are (batch * Hkv, split) pairs run one per CTA
+// at a time on `sms` CTAs; the makespan is about rounds x (key tiles per split + the
+// per-unit cost of loading Q, filling the pipeline and writing the partial result,
+// about two tiles' worth). Take the count that minimises it.
+int choose_splits(long long bhkv, int kv_tiles, int sms) {
+    int best = 1;
+    long long best_cost = -1;
+    for (int s = 1; s <= kv_tiles && s <= 256; ++s) {
+        const long long rounds = (bhkv * s + sms - 1) / sms;
+        const long long per_unit = (kv_tiles + s - 1) / s + 2;
+        const long long cost = rounds * per_unit;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+size_t decode_workspace(long long rows, int d, int splits) {
+    if (splits <= 1) return 0;
+    const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * d * sizeof(float);
+    const size_t o_pad = (o_bytes + 255) / 256 * 256;
+    return o_pad + static_cast<size_t>(splits) * static_cast<size_t>(rows) * sizeof(float);
+}
+
+int validate_decode(const void *q, const void *k, const void *v, const void *o, const float *lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window, float scale) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULLPTR;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < Nq || window < 0) return ATTN_ERR_SHAPE;
+    if (Hq % Hkv != 0) return ATTN_ERR_SHAPE;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_SHAPE;
+    if (causal != 0 && causal != 1) return ATTN_ERR_SHAPE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(Hq / Hkv) * Nq > attn::BM) return ATTN_ERR_UNSUPPORTED;  // one packed tile
+    if (Nk > (1 << 30)) return ATTN_ERR_SHAPE;
+    if (static_cast<long long>(B) * Hkv * 256 > INT_MAX) return ATTN_ERR_SHAPE;
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+        misaligned(lse, 4))
+        return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
+template <int D>
+int launch_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int causal, int window, float scale, int splits,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream, int sms) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    const int G = Hq / Hkv;
+    const int R = G * Nq;  // packed query rows per KV head
+    const long long bhkv = static_cast<long long>(B) * Hkv;
+    const int kv_tiles = (Nk + attn::BN - 1) / attn::BN;
+    if (splits <= 0) splits = choose_splits(bhkv, kv_tiles, sms);
+    if (splits > kv_tiles) splits = kv_tiles;
+    const long long rows = bhkv * R;
+    if (splits > 1) {
+        if (!workspace) return ATTN_ERR_NULLPTR;
+        if (misaligned(workspace, 256)) return ATTN_ERR_ALIGN;
+        if (workspace_bytes < decode_workspace(rows, D, splits)) return ATTN_ERR_WORKSPACE;
+    }
+    CUtensorMap mq, mk, mv, mo;
+    int rc;
+    if ((rc = encode_map(enc, &mq, q, D, R, bhkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mk, k, D, Nk, bhkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mv, v, D, Nk, bhkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mo, o, D, R, bhkv)) != ATTN_OK) return rc;
+    attn::Params p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.key_len = nullptr;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.N = R;
+    p.group = G;
+    p.causal = causal;
+    p.window = window >= Nk ? 0 : window;
+    p.sym = (p.window > 0 && !causal) ? 1 : 0;
+    p.n_kv = kv_tiles;
+    p.n_pairs = 1;
+    p.sl2 = scale * 1.4426950408889634f;
+    p.timeout_ns = attn::WAIT_LIMIT_NS;
+    p.div_bh = p.div_hq = p.div_group = attn::make_fastdiv(1u);
+    p.Nk = Nk;
+    p.pos_off = Nk - Nq;
+    p.Nq = Nq;
+    p.splits = splits;
+    // key tiles some packed row can see: from the earliest query's window start to the end
+    const int pos_min = Nk - Nq;
+    const int first_key = p.window > 0 ? (pos_min - p.window + 1 > 0 ? pos_min - p.window + 1 : 0) : 0;
+    p.split_lo = first_key / attn::BN;
+    p.split_hi = kv_tiles;
+    p.split_len = (p.split_hi - p.split_lo + splits - 1) / splits;
+    p.div_splits = attn::make_fastdiv(static_cast<uint32_t>(splits));
+    p.div_nq = attn::make_fastdiv(static_cast<uint32_t>(Nq));
+    p.num_units = static_cast<int>(bhkv * splits);
+    if (splits > 1) {
+        p.o_part = static_cast<float *>(workspace);
+        const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * D * sizeof(float);
+        p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
+    } else {
+        p.o_part = p.lse_part = nullptr;
+    }
+    const int grid = p.num_units < sms ? p.num_units : sms;
+    attn::attn_fwd_kernel<D, true><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (splits > 1) {
+        const int blocks = static_cast<int>((rows + 7) / 8);
+        attn::decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part,
+                                                                   static_cast<__nv_bfloat16 *>(o), lse,
+                                                                   static_cast<int>(rows), splits);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
     return ATTN_OK;
 }
 
@@ -1029,6 +1307,35 @@ int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float 
     if (!key_len) return ATTN_ERR_NULLPTR;
     if (misaligned(key_len, 4)) return ATTN_ERR_ALIGN;
     return fwd_common(q, k, v, o, lse, key_len, B, Hq, Hkv, N, d, causal, window, scale, stream);
+}
+
+size_t attn_fwd_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int splits) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < Nq || Hq % Hkv != 0 || (d != 64 && d != 128))
+        return 0;
+    const int kv_tiles = (Nk + attn::BN - 1) / attn::BN;
+    const long long bhkv = static_cast<long long>(B) * Hkv;
+    if (splits <= 0) {
+        int sms = 0;
+        if (device_setup(&sms) != ATTN_OK) return 0;
+        splits = choose_splits(bhkv, kv_tiles, sms);
+    }
+    if (splits > kv_tiles) splits = kv_tiles;
+    return decode_workspace(bhkv * (Hq / Hkv) * Nq, d, splits);
+}
+
+int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                    int Hkv, int Nq, int Nk, int d, int causal, int window, float scale, int splits,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = validate_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    int sms = 0;
+    if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return launch_decode<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, causal, window, scale, splits,
+                                 workspace, workspace_bytes, s, sms);
+    return launch_decode<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, causal, window, scale, splits,
+                              workspace, workspace_bytes, s, sms);
 }
 
 int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse, void *dq,
@@ -1064,6 +1371,7 @@ const char *attn_status_str(int status) {
         case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: head dim, mask or device not supported";
         case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA runtime call failed";
         case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait ran out of time";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: the workspace is smaller than required";
         default: return "unknown attn_status";
     }
 }

@@ -73,3 +73,41 @@ def make_qkv(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int,
 
 def make_workload(w: Workload):
     return make_qkv(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed, w.q_head0_scale)
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq queries per head at the end of an Nk-token sequence (key-value cache read)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    note: str = ""
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# A decode step of the GQA configuration's head layout: one new token per sequence
+# reading an 8192-token cache (memory-bound: every key and value is read once).
+DECODE_WORKLOADS = {
+    "decode_8k": DecodeWorkload("decode_8k", 8, 32, 8, 1, 8192, 128, True, 6,
+                                note="B8 Hq32 Hkv8 Nq1 Nk8192 d128 causal (decode step)"),
+}
+
+
+def make_qkv_decode(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, seed: int):
+    """(q [B,Hq,Nq,d], k [B,Hkv,Nk,d], v [B,Hkv,Nk,d]) as CPU bf16, drawn in that order
+    from one generator seeded with `seed`, N(0,1) rounded to bf16."""
+    g = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((B, Hq, Nq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32)
+    return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
+            v.to(torch.bfloat16).contiguous())

@@ -50,6 +50,7 @@
 #ifndef ATTN_API_H
 #define ATTN_API_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -65,7 +66,8 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = -4, /* d not 64 or 128; the current device is not an sm_103
                                   (B300-class) GPU */
     ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed; see attn_last_cuda_error */
-    ATTN_ERR_TIMEOUT = -6      /* a kernel wait gave up (reported by attn_device_error) */
+    ATTN_ERR_TIMEOUT = -6,     /* a kernel wait gave up (reported by attn_device_error) */
+    ATTN_ERR_WORKSPACE = -7    /* the caller's workspace is smaller than required */
 } attn_status;
 
 /*
@@ -104,6 +106,36 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float *lse,
                     const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
                     int window, float scale, void *stream);
+
+/*
+ * attn_fwd_decode -- the decode shape: Nq query rows that are the LAST Nq positions of
+ * a sequence of Nk >= Nq tokens whose keys and values are given (a key-value cache read
+ * by the newest tokens: the generation stage in the SpAtten review's "Background"
+ * section). Query row i stands at position i + Nk - Nq and the mask of attn_fwd applies
+ * to that position. With Nq = Nk it computes what attn_fwd computes.
+ *
+ *   q    device, bf16 [B, Hq,  Nq, d], 16-byte aligned (read)
+ *   k, v device, bf16 [B, Hkv, Nk, d], 16-byte aligned (read)
+ *   o    device, bf16 [B, Hq,  Nq, d], 16-byte aligned (written)
+ *   lse  device, fp32 [B, Hq,  Nq], 4-byte aligned (written; natural log)
+ *   causal, window, scale   as for attn_fwd, on positions
+ *   splits  number of parts the key sequence is divided into, each computed by its own
+ *           CTA; 0 = the library's choice for the current device (see below); values
+ *           above the number of 128-key tiles are reduced to it
+ *   workspace, workspace_bytes  device scratch owned by the caller, 256-byte aligned,
+ *           at least attn_fwd_decode_workspace_size(...) bytes; unused (may be NULL)
+ *           when the split count is 1. It holds each split's fp32 partial O and LSE,
+ *           which a second kernel merges by log-sum-exp into o and lse.
+ *
+ * The G = Hq / Hkv query heads that share a KV head are packed into one tile of
+ * G * Nq <= 128 rows (ATTN_ERR_UNSUPPORTED otherwise), so every K/V tile is read once
+ * per split for all of them. ATTN_ERR_WORKSPACE when the workspace is too small.
+ * Asynchronous on `stream`; calls that share a workspace must not overlap.
+ */
+size_t attn_fwd_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int splits);
+int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                    int Hkv, int Nq, int Nk, int d, int causal, int window, float scale, int splits,
+                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * attn_fwd_host -- the same operation for callers whose tensors live in host memory.

@@ -18,7 +18,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ea.header_functions()
-    assert set(names) >= {"attn_fwd", "attn_fwd_padded", "attn_fwd_host", "attn_status_str",
+    assert set(names) >= {"attn_fwd", "attn_fwd_padded", "attn_fwd_decode",
+                          "attn_fwd_decode_workspace_size", "attn_fwd_host", "attn_status_str",
                           "attn_last_cuda_error",
                           "attn_device_error", "attn_selftest_wait_timeout", "attn_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
@@ -30,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         s = lib.attn_status_str(code).decode()
         assert s.startswith("ATTN_")
     assert lib.attn_status_str(-99).decode() == "unknown attn_status"
@@ -73,6 +74,40 @@ def test_padded_entry_validates_key_len(lib):
     assert lib.attn_fwd_padded(*args, None, 1, 1, 1, 128, 64, 0, 0, 0.125, None) == ea.ATTN_ERR_NULLPTR
     assert lib.attn_fwd_padded(*args, A + 2, 1, 1, 1, 128, 64, 0, 0, 0.125, None) == ea.ATTN_ERR_ALIGN
     assert lib.attn_fwd_padded(*args, A, 1, 1, 1, 128, 96, 0, 0, 0.125, None) == ea.ATTN_ERR_UNSUPPORTED
+
+
+def dcall(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=4, Hkv=1, Nq=1, Nk=256, d=128, causal=1,
+          window=0, scale=0.1, splits=1, ws=None, ws_bytes=0):
+    return lib.attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, window, scale, splits,
+                               ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), ea.ATTN_ERR_NULLPTR),
+    (dict(Nq=0), ea.ATTN_ERR_SHAPE),
+    (dict(Nq=300, Nk=299), ea.ATTN_ERR_SHAPE),          # more queries than keys
+    (dict(Hq=6, Hkv=4), ea.ATTN_ERR_SHAPE),
+    (dict(Hq=64, Hkv=1, Nq=4), ea.ATTN_ERR_UNSUPPORTED),  # 256 packed rows > one tile
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(window=-2), ea.ATTN_ERR_SHAPE),
+    (dict(o=A + 8), ea.ATTN_ERR_ALIGN),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert dcall(lib, **kw) == code
+
+
+def test_decode_workspace_size(lib):
+    # one split needs none; otherwise splits x rows x (d fp32 + 1 fp32 LSE), O part
+    # padded to 256 bytes
+    assert lib.attn_fwd_decode_workspace_size(2, 8, 2, 3, 1000, 128, 1) == 0
+    rows = 2 * 2 * 4 * 3
+    o_bytes = 5 * rows * 128 * 4
+    assert lib.attn_fwd_decode_workspace_size(2, 8, 2, 3, 1000, 128, 5) == \
+        (o_bytes + 255) // 256 * 256 + 5 * rows * 4
+    # a split count above the number of 128-key tiles is reduced to it (8 tiles here)
+    assert lib.attn_fwd_decode_workspace_size(1, 4, 1, 1, 1000, 64, 50) == \
+        lib.attn_fwd_decode_workspace_size(1, 4, 1, 1, 1000, 64, 8)
+    assert lib.attn_fwd_decode_workspace_size(1, 4, 3, 1, 100, 64, 2) == 0   # bad shape
 
 
 def test_host_entry_validates_both_buffer_sets(lib):

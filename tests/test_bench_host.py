@@ -117,3 +117,13 @@ def test_max_over_two_gloo_ranks():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == {0: 1.5, 1: 1.5}
+
+
+def test_decode_accounting():
+    from exact_self_attention_fwd_b300.inputs import DecodeWorkload
+    w = DecodeWorkload("t", 2, 8, 2, 3, 10, 64, True, 0)
+    # positions 7, 8, 9 see 8, 9, 10 keys
+    assert bench.decode_flops(w) == 4 * 2 * 8 * (8 + 9 + 10) * 64
+    wb = DecodeWorkload("t", 2, 8, 2, 3, 10, 64, False, 0)
+    assert bench.decode_flops(wb) == 4 * 2 * 8 * 30 * 64
+    assert bench.decode_hbm_bytes(w) == 2 * (2 * 8 * 3 * 64 * 2) + 2 * (2 * 2 * 10 * 64 * 2) + 2 * 8 * 3 * 4
