@@ -2,14 +2,16 @@
 C-ABI library libattn_fwd.so (include/attn_api.h). PyTorch supplies device memory
 and streams; the attention itself runs only in the library's CUDA kernel.
 """
-from ._lib import (ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_NULLPTR, ATTN_ERR_SHAPE,
-                   ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_OK, AttnError,
+from ._lib import (ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_NULLPTR, ATTN_ERR_SCRATCH_LIMIT,
+                   ATTN_ERR_SHAPE, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE,
+                   ATTN_OK, AttnError,
                    attn_fwd, attn_fwd_decode, attn_fwd_host, decode_workspace_size, device_error,
                    header_functions, load, selftest_wait_timeout, status_str, version)
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_NULLPTR", "ATTN_ERR_ALIGN", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED",
-    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "AttnError", "attn_fwd",
+    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_SCRATCH_LIMIT",
+    "AttnError", "attn_fwd",
     "attn_fwd_decode", "attn_fwd_host", "decode_workspace_size", "device_error", "header_functions",
     "load", "selftest_wait_timeout", "status_str", "version",
 ]

@@ -23,6 +23,7 @@ ATTN_ERR_UNSUPPORTED = -4
 ATTN_ERR_CUDA = -5
 ATTN_ERR_TIMEOUT = -6
 ATTN_ERR_WORKSPACE = -7
+ATTN_ERR_SCRATCH_LIMIT = -8
 
 _lib = None
 
@@ -52,6 +53,8 @@ def _declare(lib):
     lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
                                     ctypes.c_size_t, vp]
     lib.attn_fwd_decode.restype = i
+    lib.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+    lib.attn_fwd_decode_noalloc.restype = i
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_host.restype = i
     lib.attn_status_str.argtypes = [i]

@@ -70,6 +70,14 @@ constexpr uint32_t WAIT_SLEEP_NS = 200000u;  // a waiting thread re-checks at le
 
 __device__ unsigned int g_status;  // bit 0: some wait ran out of time
 
+// Scratch of attn_fwd_decode_noalloc: the per-split partial results that attn_fwd_decode
+// keeps in a caller-provided workspace live here instead, in a fixed array that every
+// device holds from the moment it loads this library until the process exits. Host code
+// must not use the name as a device address: the address comes from
+// cudaGetSymbolAddress, taken once per device.
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
 // Division of a non-negative int below 2^31 by an invariant divisor d >= 1, by a
 // multiply-high and a shift (Granlund and Montgomery, "Division by invariant integers
 // using multiplication", 1994, unsigned case): with l = ceil(log2 d) and
@@ -1009,6 +1017,7 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
 thread_local int t_last_cuda_error = 0;
 
 int cuda_fail(cudaError_t e) {
@@ -1181,6 +1190,23 @@ int choose_splits(long long bhkv, int kv_tiles, int sms) {
     return best;
 }
 
+// Device address of the static scratch array on the current device. The first call on
+// a device looks it up (cudaGetSymbolAddress, with that device current) and caches it.
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        if ((e = cudaGetSymbolAddress(&ptr, attn::g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return ATTN_OK;
+}
+
 size_t decode_workspace(long long rows, int d, int splits) {
     if (splits <= 1) return 0;
     const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * d * sizeof(float);
@@ -1338,6 +1364,30 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
                               workspace, workspace_bytes, s, sms);
 }
 
+int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                            int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window, float scale,
+                            int splits, void *stream) {
+    int rc = validate_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    int sms = 0;
+    if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
+    void *scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != ATTN_OK) return rc;
+    // the same split count attn_fwd_decode would use; its partial results must fit
+    const int kv_tiles = (Nk + attn::BN - 1) / attn::BN;
+    const long long bhkv = static_cast<long long>(B) * Hkv;
+    if (splits <= 0) splits = choose_splits(bhkv, kv_tiles, sms);
+    if (splits > kv_tiles) splits = kv_tiles;
+    if (decode_workspace(bhkv * (Hq / Hkv) * Nq, d, splits) > attn::NOALLOC_SCRATCH_BYTES)
+        return ATTN_ERR_SCRATCH_LIMIT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return launch_decode<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, causal, window, scale, splits,
+                                 scratch, attn::NOALLOC_SCRATCH_BYTES, s, sms);
+    return launch_decode<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, causal, window, scale, splits,
+                              scratch, attn::NOALLOC_SCRATCH_BYTES, s, sms);
+}
+
 int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse, void *dq,
                   void *dk, void *dv, void *do_, float *dlse, int B, int Hq, int Hkv, int N, int d,
                   int causal, int window, float scale, void *stream) {
@@ -1372,6 +1422,8 @@ const char *attn_status_str(int status) {
         case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA runtime call failed";
         case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait ran out of time";
         case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: the workspace is smaller than required";
+        case ATTN_ERR_SCRATCH_LIMIT:
+            return "ATTN_ERR_SCRATCH_LIMIT: the split results need more than the fixed 8 MiB scratch";
         default: return "unknown attn_status";
     }
 }

@@ -67,7 +67,9 @@ typedef enum {
                                   (B300-class) GPU */
     ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed; see attn_last_cuda_error */
     ATTN_ERR_TIMEOUT = -6,     /* a kernel wait gave up (reported by attn_device_error) */
-    ATTN_ERR_WORKSPACE = -7    /* the caller's workspace is smaller than required */
+    ATTN_ERR_WORKSPACE = -7,   /* the caller's workspace is smaller than required */
+    ATTN_ERR_SCRATCH_LIMIT = -8 /* attn_fwd_decode_noalloc: the split results would need more
+                                   than its fixed scratch (ATTN_DECODE_NOALLOC_SCRATCH_BYTES) */
 } attn_status;
 
 /*
@@ -136,6 +138,39 @@ size_t attn_fwd_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, in
 int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
                     int Hkv, int Nq, int Nk, int d, int causal, int window, float scale, int splits,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that cannot allocate device
+ * memory. The pages have no counterpart to this entry point; it exists for users of the
+ * library.
+ *
+ * Who needs it: a caller whose device memory is fixed before it starts serving (a
+ * serving loop that reserved its whole budget at start-up and may not grow it per
+ * request), a caller running where the allocator must not be re-entered (for instance
+ * from inside a memory-pool or allocator callback), or a plain C host that holds only
+ * the tensors it passes and has no device allocator of its own. attn_fwd_decode needs
+ * a workspace for the split results; this variant needs none.
+ *
+ * Arguments and results are those of attn_fwd_decode without the workspace: the split
+ * results go to a fixed scratch array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB) that
+ * the library defines in device memory; every device holds it from the moment it loads
+ * the library until the process exits. The split count (0 = the library's choice, the
+ * same as attn_fwd_decode's) must leave splits x B x Hq x Nq x (d + 1) x 4 bytes (plus
+ * alignment) within it, else ATTN_ERR_SCRATCH_LIMIT and nothing runs; with one split
+ * the scratch is not touched.
+ *
+ * Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ * before any stream capture. Every call on a device shares the one array and each split
+ * overwrites all of its part before the merge reads it, so nothing needs clearing;
+ * calls whose kernels overlap on the GPU (different streams, or different host threads)
+ * race on it and must be serialised by the caller.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                            int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window, float scale,
+                            int splits, void *stream);
 
 /*
  * attn_fwd_host -- the same operation for callers whose tensors live in host memory.

@@ -19,7 +19,8 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = ea.header_functions()
     assert set(names) >= {"attn_fwd", "attn_fwd_padded", "attn_fwd_decode",
-                          "attn_fwd_decode_workspace_size", "attn_fwd_host", "attn_status_str",
+                          "attn_fwd_decode_workspace_size", "attn_fwd_decode_noalloc",
+                          "attn_fwd_host", "attn_status_str",
                           "attn_last_cuda_error",
                           "attn_device_error", "attn_selftest_wait_timeout", "attn_version"}
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
@@ -31,7 +32,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         s = lib.attn_status_str(code).decode()
         assert s.startswith("ATTN_")
     assert lib.attn_status_str(-99).decode() == "unknown attn_status"
