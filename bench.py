@@ -9,9 +9,10 @@ work is independent per (batch, head), so the ranks never exchange data, and the
 scaling is weak. Rank 0 prints one JSON line.
 
 Timing: W untimed warm-up calls, then K timed calls, bracketed by a barrier and a
-device synchronisation on both sides. A 256 MiB buffer is rewritten before every
-call (more than the 126 MB L2), and each call is timed by its own pair of CUDA
-events on the launching stream, so the flush is not counted. value = algorithmic
+device synchronisation on both sides. A 256 MiB buffer (more than the 126 MB L2) is
+written and then read back before every call, leaving L2 with clean lines of it,
+and each call is timed by its own pair of CUDA events on the launching stream, so
+the flush is not counted. value = algorithmic
 FLOPs of all ranks / the slowest rank's summed kernel time; FLOPs are 4 * d per
 visible (query, key) pair, masked pairs not counted.
 
@@ -41,6 +42,15 @@ from exact_self_attention_fwd_b300.inputs import (DECODE_WORKLOADS, WORKLOADS, D
 
 DEFAULT_WORKLOAD = "gqa_8k"
 FLUSH_BYTES = 256 << 20
+
+
+def flush_l2(buf):
+    """Evict L2 before a timed call: write the 256 MiB buffer (about twice the L2), then
+    read it back, so that L2 ends up holding clean lines of it; the timed call then
+    neither hits its own inputs in L2 nor pays for writing back the flush's dirty
+    lines."""
+    buf.zero_()
+    buf.view(-1, 4096).max(dim=1)
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = ["exact_self_attention_fwd_b300/csrc/attn_fwd.cu",
                   "exact_self_attention_fwd_b300/csrc/ptx.cuh"]
@@ -341,7 +351,7 @@ def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset:
     """Device time per attn_fwd call on workload w (seconds).
 
     Calls of at least a few microseconds are timed one by one with CUDA events, a
-    256 MiB rewrite between them flushing L2. The tiny workload's call is shorter
+    256 MiB write-then-read between them flushing L2. The tiny workload's call is shorter
     than the host's launch overhead, so there a CUDA graph of `steps` calls is
     replayed and timed as a whole (its 66 KB of inputs stay in L2)."""
     import torch
@@ -380,7 +390,7 @@ def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset:
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for i in range(steps):
-            flush.zero_()
+            flush_l2(flush)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
@@ -414,12 +424,63 @@ def measure_decode(ea, w: DecodeWorkload, dev, steps: int, warmup: int, seed_off
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for i in range(steps):
-            flush.zero_()
+            flush_l2(flush)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
     torch.cuda.synchronize(dev)
     return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
+
+
+def run_decode(args, w: DecodeWorkload):
+    """One JSON line for a decode-shaped workload (one GPU; HBM roofline)."""
+    import torch
+
+    import exact_self_attention_fwd_b300 as ea
+    world, rank, local = dist_env()
+    dist = init_dist(world)
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: this benchmark times the CUDA library only")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ea.load()
+    sampler = ClockSampler(nvsmi_index(local), os.path.join(args.out_dir, f"clocks_rank{rank}.csv"))
+    time.sleep(0.6)
+    barrier(dist)
+    t0 = time.time()
+    t_call = measure_decode(ea, w, dev, args.steps, args.warmup, seed_offset=rank)
+    barrier(dist)
+    t1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    if ea.device_error() != ea.ATTN_OK:
+        raise RuntimeError("kernel wait timed out")
+    t_max = max_over_ranks(dist, t_call)
+    splits_ws = ea.decode_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, 0)
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        gbs = decode_hbm_bytes(w) / t_call / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        line = {
+            "metric": "attention fwd TFLOP/s (unmasked FLOPs)", "value": decode_flops(w) * world / t_max / 1e12,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_max * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
+            "config": {"workload": w.name, "shape": w.note, "entry": "attn_fwd_decode",
+                       "l2": "256 MiB buffer written then read before every call; per-call CUDA events exclude it",
+                       "hbm_mb_per_step": decode_hbm_bytes(w) / 1e6},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": recorded_traffic(w.name),
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+                         "kernel": f"attn_fwd_kernel<{w.d}, decode>"},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": args.steps * (2 if splits_ws > 0 else 1),
+            "clocks": sampler.summary(t0, t1),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
 
 
 def run_ours(args, w: Workload):
@@ -456,7 +517,7 @@ def run_ours(args, w: Workload):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2(flush)
             call()
     torch.cuda.synchronize(dev)
     if ea.device_error() != ea.ATTN_OK:
@@ -471,7 +532,7 @@ def run_ours(args, w: Workload):
     t0 = time.time()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2(flush)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
@@ -551,7 +612,7 @@ def run_ours(args, w: Workload):
             "data": "synthetic (seeded N(0,1) rounded to bf16)",
             "config": {"workload": w.name, "shape": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                        "N": w.N, "d": w.d, "causal": w.causal, "window": w.window,
-                       "l2": "256 MiB buffer rewritten before every call; per-call CUDA events exclude it",
+                       "l2": "256 MiB buffer written then read before every call; per-call CUDA events exclude it",
                        "parallelism": f"replica per GPU x{world}",
                        "gflop_per_step": F / 1e9, "hbm_mb_per_step": hbm_bytes(w) / 1e6},
             "roofline": roof,
@@ -576,7 +637,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline field (0 = skip)")
@@ -589,6 +650,11 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     os.makedirs(args.out_dir, exist_ok=True)
+    if args.workload in DECODE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the prefill workloads"}))
+            return 0
+        return run_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
