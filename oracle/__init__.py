@@ -8,11 +8,16 @@ imports nothing from the product package.
 The arithmetic lives in ``attn_ref.c`` (plain C, fp64, one thread per slice of
 rows); this module only compiles it with gcc and marshals numpy arrays.
 
-Parity status of each function (see the pins in ``tests/test_oracle_pins.py``):
+Parity status of each function (see the pins in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_fp8.py``):
   attn_ref / attn_ref_rows -- pinned (closed forms, invariants, brute force,
   an independent library routine, and mutation tests).
   attn_ref_decode -- pinned (the last rows of the plain forward, a zero-query closed
   form, brute force and torch SDPA with an offset mask).
+  e4m3_encode / e4m3_decode / quantize_e4m3_blocks / attn_ref_fp8 -- pinned (every code
+  against torch's float8_e4m3fn, the rounding of every bf16 value in range, block
+  reconstruction bounds, exactness on representable inputs, and the block-vs-tensor
+  scaling error comparison the FlashAttention-3 review reports).
 """
 from __future__ import annotations
 
@@ -59,6 +64,18 @@ def _declare(lib):
         u16p, u16p, u16p, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
         i64p, i64, f64p, f64p, ctypes.c_int]
     lib.attn_ref_decode_rows_f64.restype = ctypes.c_int
+    lib.attn_ref_fwd_rows_f64in.argtypes = [
+        f64p, f64p, f64p, i64, i64, i64, i64, i64, ctypes.c_int, i64, ctypes.c_double,
+        i64p, i64, f64p, f64p, ctypes.c_int]
+    lib.attn_ref_fwd_rows_f64in.restype = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.attn_ref_e4m3_decode.argtypes = [u8p, i64, f64p]
+    lib.attn_ref_e4m3_decode.restype = None
+    lib.attn_ref_e4m3_encode.argtypes = [f64p, i64, u8p]
+    lib.attn_ref_e4m3_encode.restype = None
+    lib.attn_ref_quantize_e4m3_blocks.argtypes = [u16p, i64, i64, i64, i64, u8p,
+                                                  ctypes.POINTER(ctypes.c_float)]
+    lib.attn_ref_quantize_e4m3_blocks.restype = ctypes.c_int
     return lib
 
 
@@ -174,3 +191,96 @@ def attn_ref_decode(q, k, v, causal: bool = True, window: int = 0, scale: float 
     if rows_arr is None:
         return o.reshape(B, Hq, Nq, d), lse.reshape(B, Hq, Nq)
     return o, lse
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) blocks
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of e4m3 codes (uint8 array)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, dtype=np.float64)
+    load().attn_ref_e4m3_decode(c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), c.size,
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest e4m3 code (ties to even, saturating at 448) of each finite fp64 value."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(a.shape, dtype=np.uint8)
+    load().attn_ref_e4m3_encode(a.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), a.size,
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return out
+
+
+def quantize_e4m3_blocks(x, rows: int = 128):
+    """Block quantisation of bf16 x [..., N, d] (leading dims flattened to heads): codes
+    (uint8, same shape) and scales (fp32 [heads, ceil(N / rows)])."""
+    xb = _as_bits(x)
+    *lead, N, d = xb.shape
+    BH = int(np.prod(lead)) if lead else 1
+    codes = np.empty(xb.shape, dtype=np.uint8)
+    nblk = (N + rows - 1) // rows
+    scales = np.empty((BH, nblk), dtype=np.float32)
+    rc = load().attn_ref_quantize_e4m3_blocks(
+        xb.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), BH, N, d, rows,
+        codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+        scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return codes, scales
+
+
+def dequantize_e4m3_blocks(codes, scales, rows: int = 128) -> np.ndarray:
+    """fp64 code x scale of each element."""
+    c = np.asarray(codes)
+    *lead, N, d = c.shape
+    BH = int(np.prod(lead)) if lead else 1
+    vals = e4m3_decode(c).reshape(BH, N, d)
+    sc = np.asarray(scales, dtype=np.float64).reshape(BH, -1)
+    blk = np.arange(N) // rows
+    return (vals * sc[:, blk][:, :, None]).reshape(c.shape)
+
+
+def attn_ref_f64in(q, k, v, causal: bool = False, window: int = 0, scale: float = 1.0,
+                   rows=None, nthreads: int | None = None):
+    """The plain forward on fp64 inputs q [B,Hq,N,d], k/v [B,Hkv,N,d]."""
+    qa, ka, va = (np.ascontiguousarray(np.asarray(t, dtype=np.float64)) for t in (q, k, v))
+    B, Hq, N, d = qa.shape
+    Hkv = ka.shape[1]
+    rows_arr = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = B * Hq * N if rows_arr is None else rows_arr.size
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = load().attn_ref_fwd_rows_f64in(
+        qa.ctypes.data_as(f64p), ka.ctypes.data_as(f64p), va.ctypes.data_as(f64p), B, Hq, Hkv, N, d,
+        int(bool(causal)), int(window), float(scale),
+        rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
+        nrows, o.ctypes.data_as(f64p), lse.ctypes.data_as(f64p), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    if rows_arr is None:
+        return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)
+    return o, lse
+
+
+def attn_ref_fp8(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
+                 rows=None, block_rows: int = 128, per_tensor: bool = False):
+    """FP8 attention as the FlashAttention-3 review describes it: Q, K and V are block
+    quantised to e4m3 (blocks of block_rows x d per head, or one scale for the whole
+    tensor when per_tensor), then attention is computed exactly (fp64) on the
+    dequantised values. Returns (o, lse) like attn_ref, plus the dequantised inputs."""
+    d = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    deq = []
+    for t in (q, k, v):
+        if per_tensor:
+            flat = t.reshape(1, 1, -1, d)
+            codes, sc = quantize_e4m3_blocks(flat, rows=flat.shape[2])
+            deq.append(dequantize_e4m3_blocks(codes, sc, rows=flat.shape[2]).reshape(tuple(t.shape)))
+        else:
+            codes, sc = quantize_e4m3_blocks(t, rows=block_rows)
+            deq.append(dequantize_e4m3_blocks(codes, sc, rows=block_rows))
+    o, lse = attn_ref_f64in(deq[0], deq[1], deq[2], causal, window, scale, rows)
+    return o, lse, deq

@@ -75,6 +75,7 @@ static int key_visible(int64_t i, int64_t j, int causal, int64_t window, int64_t
 
 typedef struct {
     const uint16_t *q, *k, *v;
+    const double *qd64, *kd64, *vd64;   /* fp64 inputs instead of bf16 bits, when set */
     int64_t B, Hq, Hkv, N, d;   /* N: query rows per head */
     int64_t Nk;                 /* keys per head; query row i stands at i + Nk - N */
     int causal;
@@ -101,20 +102,26 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
     if (L > Nk) L = Nk;
     const int64_t pos = i + (Nk - N);   /* position of query row i in the sequence */
 
-    const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;
-    const uint16_t *kbase = jb->k + (b * jb->Hkv + kv) * Nk * d;
-    const uint16_t *vbase = jb->v + (b * jb->Hkv + kv) * Nk * d;
+    const int64_t qoff = ((b * jb->Hq + hq) * N + i) * d;
+    const int64_t kvoff = (b * jb->Hkv + kv) * Nk * d;
+    const uint16_t *qrow = jb->q ? jb->q + qoff : NULL;
+    const uint16_t *kbase = jb->k ? jb->k + kvoff : NULL;
+    const uint16_t *vbase = jb->v ? jb->v + kvoff : NULL;
+    const double *qrow64 = jb->qd64 ? jb->qd64 + qoff : NULL;
+    const double *kbase64 = jb->kd64 ? jb->kd64 + kvoff : NULL;
+    const double *vbase64 = jb->vd64 ? jb->vd64 + kvoff : NULL;
+#define KVAL(j, c) (kbase64 ? kbase64[(j) * d + (c)] : bf16_bits_to_double(kbase[(j) * d + (c)]))
+#define VVAL(j, c) (vbase64 ? vbase64[(j) * d + (c)] : bf16_bits_to_double(vbase[(j) * d + (c)]))
 
-    for (int64_t c = 0; c < d; ++c) qd[c] = bf16_bits_to_double(qrow[c]);
+    for (int64_t c = 0; c < d; ++c) qd[c] = qrow64 ? qrow64[c] : bf16_bits_to_double(qrow[c]);
 
     /* scores over the visible keys */
     double m = -INFINITY;
     int64_t nvis = 0;
     for (int64_t j = 0; j < Nk; ++j) {
         if (!key_visible(pos, j, jb->causal, jb->window, L)) continue;
-        const uint16_t *krow = kbase + j * d;
         double dot = 0.0;
-        for (int64_t c = 0; c < d; ++c) dot += qd[c] * bf16_bits_to_double(krow[c]);
+        for (int64_t c = 0; c < d; ++c) dot += qd[c] * KVAL(j, c);
         s[j] = jb->scale * dot;
         if (s[j] > m) m = s[j];
         ++nvis;
@@ -138,9 +145,10 @@ static void one_row(const job_t *jb, int64_t flat, double *o_row, double *lse_ou
     for (int64_t j = 0; j < Nk; ++j) {
         if (!key_visible(pos, j, jb->causal, jb->window, L)) continue;
         const double p = exp(s[j] - lse);
-        const uint16_t *vrow = vbase + j * d;
-        for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_bits_to_double(vrow[c]);
+        for (int64_t c = 0; c < d; ++c) o_row[c] += p * VVAL(j, c);
     }
+#undef KVAL
+#undef VVAL
 }
 
 static void *worker(void *arg) {
@@ -174,10 +182,11 @@ static int check_args(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
  * arguments (-1 null pointer, -3 shape, -4 unsupported combination).
  */
 static int rows_core(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const double *q64, const double *k64, const double *v64,
                      int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t Nk, int64_t d,
                      int causal, int64_t window, double scale, const int32_t *key_len,
                      const int64_t *rows, int64_t nrows, double *o, double *lse, int nthreads) {
-    if (!q || !k || !v || !o || !lse) return -1;
+    if (!(q || q64) || !(k || k64) || !(v || v64) || !o || !lse) return -1;
     int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
     if (rc) return rc;
     if (Nk < N) return -3;
@@ -201,6 +210,7 @@ static int rows_core(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     for (int t = 0; t < nthreads; ++t) {
         job_t *jb = &jobs[t];
         jb->q = q; jb->k = k; jb->v = v;
+        jb->qd64 = q64; jb->kd64 = k64; jb->vd64 = v64;
         jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d; jb->Nk = Nk;
         jb->causal = causal; jb->window = window; jb->scale = scale;
         jb->key_len = key_len;
@@ -230,8 +240,8 @@ int attn_ref_fwd_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *
                           int causal, int64_t window, double scale, const int32_t *key_len,
                           const int64_t *rows, int64_t nrows, double *o, double *lse,
                           int nthreads) {
-    return rows_core(q, k, v, B, Hq, Hkv, N, N, d, causal, window, scale, key_len, rows, nrows,
-                     o, lse, nthreads);
+    return rows_core(q, k, v, NULL, NULL, NULL, B, Hq, Hkv, N, N, d, causal, window, scale, key_len,
+                     rows, nrows, o, lse, nthreads);
 }
 
 /* Decode shape: q [B,Hq,Nq,d], k and v [B,Hkv,Nk,d], Nk >= Nq; rows are flat ids
@@ -241,8 +251,8 @@ int attn_ref_decode_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_
                              int causal, int64_t window, double scale,
                              const int64_t *rows, int64_t nrows, double *o, double *lse,
                              int nthreads) {
-    return rows_core(q, k, v, B, Hq, Hkv, Nq, Nk, d, causal, window, scale, NULL, rows, nrows,
-                     o, lse, nthreads);
+    return rows_core(q, k, v, NULL, NULL, NULL, B, Hq, Hkv, Nq, Nk, d, causal, window, scale, NULL,
+                     rows, nrows, o, lse, nthreads);
 }
 
 /* All rows: o is [B,Hq,N,d], lse is [B,Hq,N], both fp64. key_len may be NULL. */
@@ -252,4 +262,96 @@ int attn_ref_fwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      double *o, double *lse, int nthreads) {
     return attn_ref_fwd_rows_f64(q, k, v, B, Hq, Hkv, N, d, causal, window, scale, key_len,
                                  NULL, B * Hq * N, o, lse, nthreads);
+}
+
+/* Plain forward on fp64 inputs (q [B,Hq,N,d], k and v [B,Hkv,N,d]): the same definition,
+ * for inputs that are not bf16 values (for instance dequantised FP8 blocks). */
+int attn_ref_fwd_rows_f64in(const double *q, const double *k, const double *v,
+                            int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                            int causal, int64_t window, double scale,
+                            const int64_t *rows, int64_t nrows, double *o, double *lse,
+                            int nthreads) {
+    return rows_core(NULL, NULL, NULL, q, k, v, B, Hq, Hkv, N, N, d, causal, window, scale, NULL,
+                     rows, nrows, o, lse, nthreads);
+}
+
+/*
+ * FP8 (e4m3) block quantisation, after the FlashAttention-3 review's "Block
+ * Quantization" and FP8 answers (deepmi.me): e4m3 has a sign bit, a 4-bit exponent and
+ * a 3-bit mantissa; Q, K and V are split into blocks of B_r rows x d, each block gets
+ * its own scale from its largest magnitude, and the scaled values are rounded to FP8.
+ *
+ * The e4m3 encoding used here (the OCP "E4M3FN" variant): exponent bias 7, no infinity,
+ * the all-ones pattern S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 x 2^8 = 448; exponent field 0 holds subnormals m/8 x 2^-6. Rounding is to
+ * nearest, ties to even, and magnitudes beyond 448 saturate to 448.
+ */
+static double e4m3_value(uint8_t code) {
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Round x (finite) to the nearest e4m3 value, ties to the even code; saturate at 448. */
+static uint8_t e4m3_round(double x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);  /* 448 = 1.75 x 2^8 */
+    /* candidates: the two representable magnitudes around a, by exhaustive search over
+     * the 127 non-negative finite codes (simple and obviously correct) */
+    uint8_t best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = (uint8_t)c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void attn_ref_e4m3_decode(const uint8_t *codes, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+void attn_ref_e4m3_encode(const double *x, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_round(x[i]);
+}
+
+/*
+ * Block quantisation of a bf16 tensor [BH, N, d] in blocks of `rows` x d: for block k of
+ * head h, amax = max |x| (as fp32), inv = 448 / amax computed in fp32 (1 when amax is
+ * 0), code = e4m3(x * inv) with the product rounded to fp32 first, and the block's
+ * scale = amax / 448 in fp32 (the dequantised value is code x scale). Writes codes
+ * [BH, N, d] and scales [BH, ceil(N / rows)].
+ */
+int attn_ref_quantize_e4m3_blocks(const uint16_t *x, int64_t BH, int64_t N, int64_t d, int64_t rows,
+                                  uint8_t *codes, float *scales) {
+    if (!x || !codes || !scales || BH < 1 || N < 1 || d < 1 || rows < 1) return -1;
+    const int64_t nblk = (N + rows - 1) / rows;
+    for (int64_t h = 0; h < BH; ++h) {
+        for (int64_t k = 0; k < nblk; ++k) {
+            const int64_t r0 = k * rows, r1 = (r0 + rows < N) ? r0 + rows : N;
+            float amax = 0.0f;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c) {
+                    const float a = fabsf((float)bf16_bits_to_double(x[(h * N + r) * d + c]));
+                    if (a > amax) amax = a;
+                }
+            const float inv = (amax > 0.0f) ? 448.0f / amax : 1.0f;
+            scales[h * nblk + k] = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c) {
+                    const volatile float prod = (float)bf16_bits_to_double(x[(h * N + r) * d + c]) * inv;
+                    codes[(h * N + r) * d + c] = e4m3_round((double)prod);
+                }
+        }
+    }
+    return 0;
 }

@@ -23,12 +23,12 @@ MUTANTS = {
     # a dropped term in the log-sum-exp
     "lse_drops_max": ("const double lse = m + log(l);", "const double lse = log(l);"),
     # transposed operands: the score uses V rows instead of K rows
-    "scores_from_v": ("const uint16_t *krow = kbase + j * d;", "const uint16_t *krow = vbase + j * d;"),
+    "scores_from_v": ("dot += qd[c] * KVAL(j, c);", "dot += qd[c] * VVAL(j, c);"),
     # a wrong sign in the probability
     "probability_sign": ("const double p = exp(s[j] - lse);", "const double p = exp(lse - s[j]);"),
     # wrong query row index (row-major stride slip)
-    "query_row_index": ("const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i) * d;",
-                        "const uint16_t *qrow = jb->q + ((b * jb->Hq + hq) * N + i / 2) * d;"),
+    "query_row_index": ("const int64_t qoff = ((b * jb->Hq + hq) * N + i) * d;",
+                        "const int64_t qoff = ((b * jb->Hq + hq) * N + i / 2) * d;"),
     # padded query rows are not masked (only padded keys are)
     "padding_rows_unmasked": ("if (i >= L || j >= L) return 0;", "if (j >= L) return 0;"),
     # padded keys are not masked
