@@ -432,6 +432,47 @@ def measure_decode(ea, w: DecodeWorkload, dev, steps: int, warmup: int, seed_off
     return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
 
 
+def measure_fp8(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
+    """Device time per call of (a) attn_fwd_fp8 on pre-quantised operands and (b) the
+    block quantisation of Q, K and V (three attn_quantize_e4m3 calls), per-call CUDA
+    events with L2 flushed between calls."""
+    import torch
+    q, k, v = make_qkv(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed + seed_offset, w.q_head0_scale)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        (q8, qs), (k8, ks), (v8, vs) = (ea.quantize_e4m3(t, stream=stream) for t in (qd, kd, vd))
+    out = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+
+    def attn():
+        ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=w.causal, window=w.window, scale=w.scale, out=out,
+                        lse=lse, stream=stream)
+
+    def quant():
+        for t in (qd, kd, vd):
+            ea.quantize_e4m3(t, stream=stream)
+
+    res = []
+    for fn in (attn, quant):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                flush_l2(flush)
+                starts[i].record(stream)
+                fn()
+                ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        res.append(sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps)
+    return res[0], res[1]
+
+
 def run_decode(args, w: DecodeWorkload):
     """One JSON line for a decode-shaped workload (one GPU; HBM roofline)."""
     import torch
@@ -588,6 +629,17 @@ def run_ours(args, w: Workload):
             summary[name] = {"tflops": flops(ww) / t_call / 1e12, "us_per_call": t_call * 1e6,
                              "gbs": hbm_bytes(ww) / t_call / 1e9, "bound": r["bound"],
                              "frac": r["frac"], "timing": how}
+        fw = WORKLOADS["gqa_8k"]
+        t_attn, t_quant = measure_fp8(ea, fw, dev, args.summary_steps, 5, seed_offset=rank)
+        fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        qbytes = (fw.B * fw.Hq + 2 * fw.B * fw.Hkv) * fw.N * fw.d * 3  # read bf16, write e4m3
+        summary["gqa_8k_fp8"] = {
+            "tflops": flops(fw) / t_attn / 1e12, "us_per_call": t_attn * 1e6, "bound": "tensor",
+            "frac": flops(fw) / t_attn / 1e12 / fp8_peak,
+            "peak_note": "fp8 peak = 2 x measured bf16 burst peak (nominal dense ratio)",
+            "quantize_us": t_quant * 1e6, "quantize_gbs": qbytes / t_quant / 1e9,
+            "timing": "per-call CUDA events, L2 flushed between calls",
+            "entry": "attn_fwd_fp8 (e4m3 Q, K, V with 128-row block scales); attn_quantize_e4m3 timed apart"}
         for name, dw in DECODE_WORKLOADS.items():
             t_call = measure_decode(ea, dw, dev, args.summary_steps, 5, seed_offset=rank)
             gbs = decode_hbm_bytes(dw) / t_call / 1e9

@@ -55,6 +55,10 @@ def _declare(lib):
     lib.attn_fwd_decode.restype = i
     lib.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
     lib.attn_fwd_decode_noalloc.restype = i
+    lib.attn_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, vp]
+    lib.attn_quantize_e4m3.restype = i
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_fwd_fp8.restype = i
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_host.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -200,6 +204,58 @@ def attn_fwd_decode(q, k, v, causal: bool = True, window: int = 0, scale: float 
         rc = L.attn_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), int(window), float(scale),
                                int(splits), ws_ptr, ws_bytes, _stream_handle(stream, dev))
+    _check(rc)
+    return out, lse
+
+
+def quantize_e4m3(x, stream=None):
+    """Block quantisation of a CUDA bf16 tensor [..., N, d] (d = 64 or 128) to e4m3 codes
+    (uint8, same shape) and fp32 scales [heads, ceil(N / 128)] (attn_quantize_e4m3)."""
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.device.type != "cuda" or x.dim() < 2:
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [..., N, d]")
+    N, d = x.shape[-2], x.shape[-1]
+    BH = x.numel() // (N * d)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((BH, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = load().attn_quantize_e4m3(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), BH, N, d,
+                                       _stream_handle(stream, x.device))
+    _check(rc)
+    return codes, scales
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, window: int = 0,
+                 scale: float | None = None, out=None, lse=None, stream=None):
+    """Attention forward on e4m3 operands with per-block scales (attn_fwd_fp8): q8
+    [B,Hq,N,128], k8/v8 [B,Hkv,N,128] uint8 codes, scales fp32 [B*H, ceil(N/128)] as
+    quantize_e4m3 makes them. Returns (o bf16 [B,Hq,N,128], lse fp32 [B,Hq,N])."""
+    import torch
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.dtype != torch.uint8 or not t.is_contiguous() or t.device.type != "cuda" or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D uint8 CUDA tensor")
+    for name, t in (("q_scale", q_scale), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    B, Hq, N, d = q8.shape
+    Hkv = k8.shape[1]
+    if k8.shape != v8.shape or k8.shape[0] != B or k8.shape[2] != N or k8.shape[3] != d:
+        raise ValueError("k8 and v8 must be [B, Hkv, N, d] matching q8")
+    nblk = (N + 127) // 128
+    if q_scale.numel() != B * Hq * nblk or k_scale.numel() != B * Hkv * nblk or v_scale.numel() != B * Hkv * nblk:
+        raise ValueError("scales must have one entry per 128-row block of every head")
+    dev = q8.device
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        rc = load().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), q_scale.data_ptr(),
+                                 k_scale.data_ptr(), v_scale.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+                                 _stream_handle(stream, dev))
     _check(rc)
     return out, lse
 

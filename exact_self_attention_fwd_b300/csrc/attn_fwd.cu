@@ -120,23 +120,30 @@ struct Params {
     int Nq, splits, split_lo, split_len, split_hi;
     FastDiv div_splits, div_nq;
     float *o_part, *lse_part;  // partial results per split (splits > 1), fp32
+    // e4m3 operands: per-block scales [z index][ceil(N / 128)] of Q, K and V
+    const float *q_scale, *k_scale, *v_scale;
 };
 
-template <int D>
+// F8: Q, K and V are e4m3 codes (1 byte) instead of bf16 (2 bytes); O stays bf16.
+template <int D, bool F8 = false>
 struct Cfg {
-    static constexpr int STAGES = (D == 128) ? 4 : 8;
-    static constexpr int CHUNK_BYTES = BM * 64 * 2;  // one 64-column, 128-byte-swizzled slab
-    static constexpr int NCHUNK = D / 64;
+    static constexpr int ELEM = F8 ? 1 : 2;                 // bytes per Q/K/V element
+    static constexpr int KSTEP = F8 ? 32 : 16;              // reduction length of one MMA
+    static constexpr int CHUNK_COLS = 128 / ELEM;           // columns of one 128-byte swizzled row
+    static constexpr int CHUNK_BYTES = BM * 128;            // one slab: 128 rows x 128 bytes
+    static constexpr int NCHUNK = D / CHUNK_COLS;
     static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
+    static constexpr int STAGES = (D == 128 && !F8) ? 4 : 8;
     // Q tiles of Q_BUFS units: with two, the producer loads the next unit's Q while the
-    // current unit still computes (d = 64, where shared memory has room for it).
-    static constexpr int Q_BUFS = (D == 64) ? 2 : 1;
+    // current unit still computes (where shared memory has room for it).
+    static constexpr int Q_BUFS = (D == 64 || F8) ? 2 : 1;
     static constexpr int SMEM_Q = 0;
     static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
-    // one 64-column staging block per softmax warpgroup: O goes registers -> shared
+    // one 64-column staging block per softmax warpgroup: O (bf16) goes registers -> shared
     // memory (128-byte-swizzled, like the TMA loads) -> global by a TMA tensor store
+    static constexpr int STAGE_BYTES = BM * 64 * 2;
     static constexpr int SMEM_STAGE = SMEM_KV + STAGES * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_STAGE + 2 * CHUNK_BYTES;
+    static constexpr int SMEM_BAR = SMEM_STAGE + 2 * STAGE_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
     static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
@@ -160,7 +167,9 @@ struct Cfg {
     // soon as the softmax warps have read S_t(j), while they are still turning it into
     // P. Otherwise (d = 128) P overwrites the first half of its S block, and S_t(j+1)
     // must wait until the P.V product of tile j has read P.
-    static constexpr bool SEP_P = (256 + 2 * D + 2 * 64) <= (int)TMEM_COLS;
+    static constexpr bool SEP_P = !F8 && (256 + 2 * D + 2 * 64) <= (int)TMEM_COLS;
+    // tensor-memory columns that hold one tile's P: 128 keys, 2 (bf16) or 4 (e4m3) per column
+    static constexpr int P_COLS = BN * ELEM / 4;
     static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
     static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -340,13 +349,14 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const Params &p) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool DEC>
+template <int D, bool DEC, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const Params p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, F8>;
+    static_assert(!F8 || (D == 128 && !DEC), "e4m3 operands: d = 128, plain forward");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -431,13 +441,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < C::NCHUNK; ++c)
                     ptx::tma_load_3d_elect(qdst + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 2 * qb + 0),
-                                           c * 64, q0a, zq);
+                                           c * C::CHUNK_COLS, q0a, zq);
                 if (has1) {
                     ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 2 * qb + 1), C::TILE_BYTES);
 #pragma unroll
                     for (int c = 0; c < C::NCHUNK; ++c)
                         ptx::tma_load_3d_elect(qdst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
-                                               bar(C::B_QFULL + 2 * qb + 1), c * 64, q0b, zq);
+                                               bar(C::B_QFULL + 2 * qb + 1), c * C::CHUNK_COLS, q0b, zq);
                 } else if (lane == 0) {
                     // no second tile: complete the phase anyway, so that both barriers of a
                     // buffer always advance together
@@ -455,7 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int c = 0; c < C::NCHUNK; ++c)
                             ptx::tma_load_3d_elect(sb + C::SMEM_KV + st * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                                   m, bar(C::B_KVFULL + st), c * 64, j * BN, zkv);
+                                                   m, bar(C::B_KVFULL + st), c * C::CHUNK_COLS, j * BN, zkv);
                         ++kv_it;
                     }
                 }
@@ -479,8 +489,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // All 32 lanes run this loop with identical values (so descriptors and tensor
             // memory addresses are warp-uniform); each MMA and commit is issued by one
             // elected lane.
-            constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, true);
+            constexpr uint32_t IDESC_S = F8 ? ptx::idesc_e4m3_f32(BM, BN, false) : ptx::idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t IDESC_PV = F8 ? ptx::idesc_e4m3_f32(BM, D, true) : ptx::idesc_bf16_f32(BM, D, true);
             uint32_t kv_it = 0, q_use = 0, p_use0 = 0, p_use1 = 0;
             uint32_t sf_use0 = 0, sf_use1 = 0;
             bool ok = true;
@@ -492,9 +502,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
                 const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < D / C::KSTEP; ++kk) {
+                    // each step covers 32 bytes of a 128-byte row; four steps per slab
                     const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                    ptx::mma_ss_elect(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    if constexpr (F8)
+                        ptx::mma_ss_elect_f8(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    else
+                        ptx::mma_ss_elect(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory.
@@ -510,10 +524,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_warp(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
                     ptx::tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < BN / 32; ++kk) {
-                        const int k16 = h * (BN / 32) + kk;
-                        ptx::mma_ts_elect(tmem + col_o, tmem + col_s + k16 * 8, vd + ((k16 * 2048) >> 4),
-                                          IDESC_PV, (accumulate || k16 > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / C::KSTEP / 2; ++kk) {
+                        // step k16 reads 8 tensor-memory columns of P (KSTEP keys) and the
+                        // KSTEP rows of V after the previous steps' KSTEP * 128 bytes
+                        const int k16 = h * (BN / C::KSTEP / 2) + kk;
+                        const uint64_t vstep = vd + ((k16 * C::KSTEP * 128) >> 4);
+                        if constexpr (F8)
+                            ptx::mma_ts_elect_f8(tmem + col_o, tmem + col_s + k16 * 8, vstep, IDESC_PV,
+                                                 (accumulate || k16 > 0) ? 1u : 0u);
+                        else
+                            ptx::mma_ts_elect(tmem + col_o, tmem + col_s + k16 * 8, vstep, IDESC_PV,
+                                              (accumulate || k16 > 0) ? 1u : 0u);
                     }
                 }
                 return true;
@@ -664,8 +685,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
         const uint32_t t_p = tmem + lane_off + (t ? C::COL_P1 : C::COL_P0);
-        uint8_t *stage_ptr = smem + C::SMEM_STAGE + t * C::CHUNK_BYTES;
-        const uint32_t stage_addr = sb + C::SMEM_STAGE + t * C::CHUNK_BYTES;
+        uint8_t *stage_ptr = smem + C::SMEM_STAGE + t * C::STAGE_BYTES;
+        const uint32_t stage_addr = sb + C::SMEM_STAGE + t * C::STAGE_BYTES;
         const bool store_thread = (quad == 0 && lane == 0);  // issues this warpgroup's O stores
         const uint32_t bar_efree = bar(C::B_EFREE + t), bar_efull = bar(C::B_EFULL + t);
         uint32_t e_use = 0;
@@ -694,6 +715,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int pos_first = DEC ? p.pos_off : q0;
             const int pos_last = DEC ? p.Nk - 1 : q0 + BM - 1;
             const bool padded_rows = DEC ? false : (L < p.N && q0 + BM > L);
+            // e4m3 operands: S carries the factor q_scale x k_scale of its two blocks, and
+            // the V block scales are folded into P relative to the head's largest one
+            // (P' = P x v_scale_j / v_max <= 256), so that O = v_max x sum P' V8 / sum P
+            float q_sc = 1.f, v_max = 1.f;
+            if constexpr (F8) {
+                q_sc = __ldg(p.q_scale + static_cast<size_t>(ui.zq) * p.n_kv + (q0 / BM));
+                float vm = 0.f;
+                for (int jj = lane; jj < p.n_kv; jj += 32)
+                    vm = fmaxf(vm, __ldg(p.v_scale + static_cast<size_t>(ui.zkv) * p.n_kv + jj));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+                v_max = vm;
+            }
             float m_run = -INFINITY;  // running max of scale*s*log2(e)
             float l_run = 0.f;        // running sum of 2^(x - m_run), for the LSE
             float r_run = 0.f;        // running sum of bf16(2^(x - m_run)), for normalising O
@@ -746,7 +780,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         a = ptx::fmax3(a, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
                     mxc[c] = fmaxf(a, __uint_as_float(sr[c][31]));
                 }
-                const float mx = ptx::fmax3(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * sl2;
+                float c_tile = sl2, log_ratio = 0.f, inv_ratio = 1.f;
+                if constexpr (F8) {
+                    const size_t kb = static_cast<size_t>(ui.zkv) * p.n_kv + j;
+                    c_tile = sl2 * q_sc * __ldg(p.k_scale + kb);
+                    const float ratio = __ldg(p.v_scale + kb) / v_max;
+                    log_ratio = ptx::lg2(ratio);
+                    inv_ratio = 1.f / ratio;
+                }
+                const float mx = ptx::fmax3(mxc[0], mxc[1], fmaxf(mxc[2], mxc[3])) * c_tile;
                 float m_new = m_run;
                 if (mx > m_run + RESCALE_THRESHOLD) m_new = mx;
                 const float alpha = (m_new == m_run) ? 1.f : ptx::ex2(m_run - m_new);
@@ -783,39 +825,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // sum of the ROUNDED P, by which O is normalised: O is then an exact convex
                 // combination of V rows under the weights the tensor core actually used,
                 // so the rounding of a dominant weight cancels instead of showing in O.
-                const float2 sl2x2 = make_float2(sl2, sl2);
-                const float2 negm = make_float2(-mref, -mref);
+                const float2 sl2x2 = make_float2(c_tile, c_tile);
+                const float2 negm = make_float2(log_ratio - mref, log_ratio - mref);
                 float2 le0 = make_float2(0.f, 0.f), le1 = make_float2(0.f, 0.f);
                 float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
 #pragma unroll
                     for (int c = 2 * h; c < 2 * h + 2; ++c) {
-                        uint32_t pk[16];
+                        if constexpr (F8) {
+                            // four e4m3 codes per tensor-memory column (key k in byte k % 4)
+                            uint32_t pk[8];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 x = make_float2(__uint_as_float(sr[c][2 * e]),
-                                                         __uint_as_float(sr[c][2 * e + 1]));
-                            const float2 a = __ffma2_rn(x, sl2x2, negm);
-                            const float2 pe = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-                            pk[e] = ptx::pack_bf16x2(pe.x, pe.y);
-                            if (e & 1) {
-                                le1 = __fadd2_rn(le1, pe);
-                                ptx::add_bf16x2_halves(lr2, lr3, pk[e]);
-                            } else {
-                                le0 = __fadd2_rn(le0, pe);
-                                ptx::add_bf16x2_halves(lr0, lr1, pk[e]);
+                            for (int e = 0; e < 8; ++e) {
+                                const float2 x01 = make_float2(__uint_as_float(sr[c][4 * e]),
+                                                               __uint_as_float(sr[c][4 * e + 1]));
+                                const float2 x23 = make_float2(__uint_as_float(sr[c][4 * e + 2]),
+                                                               __uint_as_float(sr[c][4 * e + 3]));
+                                const float2 a01 = __ffma2_rn(x01, sl2x2, negm);
+                                const float2 a23 = __ffma2_rn(x23, sl2x2, negm);
+                                const float2 p01 = make_float2(ptx::ex2(a01.x), ptx::ex2(a01.y));
+                                const float2 p23 = make_float2(ptx::ex2(a23.x), ptx::ex2(a23.y));
+                                pk[e] = ptx::pack_e4m3x4(p01.x, p01.y, p23.x, p23.y);
+                                le0 = __fadd2_rn(le0, p01);
+                                le1 = __fadd2_rn(le1, p23);
+                                if (e & 1)
+                                    ptx::add_e4m3x4(lr2, lr3, pk[e]);
+                                else
+                                    ptx::add_e4m3x4(lr0, lr1, pk[e]);
                             }
+                            ptx::tmem_st8(t_p + 8 * c, pk);
+                        } else {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 x = make_float2(__uint_as_float(sr[c][2 * e]),
+                                                             __uint_as_float(sr[c][2 * e + 1]));
+                                const float2 a = __ffma2_rn(x, sl2x2, negm);
+                                const float2 pe = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                                pk[e] = ptx::pack_bf16x2(pe.x, pe.y);
+                                if (e & 1) {
+                                    le1 = __fadd2_rn(le1, pe);
+                                    ptx::add_bf16x2_halves(lr2, lr3, pk[e]);
+                                } else {
+                                    le0 = __fadd2_rn(le0, pe);
+                                    ptx::add_bf16x2_halves(lr0, lr1, pk[e]);
+                                }
+                            }
+                            ptx::tmem_st16(t_p + 16 * c, pk);
                         }
-                        ptx::tmem_st16(t_p + 16 * c, pk);
                     }
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(h ? bar_p1 : bar_p0);
                 }
-                l_run = l_run * alpha + ((le0.x + le0.y) + (le1.x + le1.y));
-                r_run = r_run * alpha + ((lr0 + lr1) + (lr2 + lr3));
+                // (with e4m3 operands the sums are of P' = P x ratio: back to P's units)
+                l_run = l_run * alpha + ((le0.x + le0.y) + (le1.x + le1.y)) * inv_ratio;
+                r_run = r_run * alpha + ((lr0 + lr1) + (lr2 + lr3)) * inv_ratio;
             }
             if (!ok) break;
             if (!empty) {
@@ -826,7 +893,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             // epilogue: O / (sum of rounded P) -> bf16 -> staging block -> TMA store (rows
             // past the sequence end are clipped by the store), and the natural-log LSE
-            const float inv_l = r_run > 0.f ? 1.f / r_run : 0.f;
+            const float inv_l = r_run > 0.f ? v_max / r_run : 0.f;
             const size_t ridx = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
@@ -923,6 +990,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Block quantisation to e4m3 (the FlashAttention-3 review's "Block Quantization": each
+// B_r x d block gets its own scale from its largest magnitude, then the scaled values
+// are rounded to FP8). One CTA per (block of 128 rows, head): amax = max |x|,
+// inv = 448 / amax, code = e4m3(x * inv) rounded to nearest even with saturation, and
+// scale = amax / 448; an all-zero block gets scale 1. The division and product are
+// plain IEEE fp32 operations, so the codes are reproducible bit for bit.
+template <int D>
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                            uint8_t *__restrict__ codes,
+                                                            float *__restrict__ scales, int N, int nblk) {
+    constexpr int GROUPS = BM * D / 8 / 256;  // 8-element groups per thread
+    const int blk = blockIdx.x, h = blockIdx.y;
+    const int r0 = blk * BM;
+    const int n = min(BM, N - r0) * D;  // elements in this block
+    const size_t base = (static_cast<size_t>(h) * N + r0) * D;
+    uint4 v[GROUPS];
+    float amax = 0.f;
+#pragma unroll
+    for (int g = 0; g < GROUPS; ++g) {
+        const int e0 = (threadIdx.x + g * 256) * 8;
+        if (e0 < n) {
+            v[g] = *reinterpret_cast<const uint4 *>(x + base + e0);
+            const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+                amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+            }
+        }
+    }
+    __shared__ float red[8];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+    if (threadIdx.x == 0) scales[static_cast<size_t>(h) * nblk + blk] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+#pragma unroll
+    for (int g = 0; g < GROUPS; ++g) {
+        const int e0 = (threadIdx.x + g * 256) * 8;
+        if (e0 < n) {
+            const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+            uint2 out;
+            out.x = ptx::pack_e4m3x4(__fmul_rn(__uint_as_float(w[0] << 16), inv),
+                                     __fmul_rn(__uint_as_float(w[0] & 0xFFFF0000u), inv),
+                                     __fmul_rn(__uint_as_float(w[1] << 16), inv),
+                                     __fmul_rn(__uint_as_float(w[1] & 0xFFFF0000u), inv));
+            out.y = ptx::pack_e4m3x4(__fmul_rn(__uint_as_float(w[2] << 16), inv),
+                                     __fmul_rn(__uint_as_float(w[2] & 0xFFFF0000u), inv),
+                                     __fmul_rn(__uint_as_float(w[3] << 16), inv),
+                                     __fmul_rn(__uint_as_float(w[3] & 0xFFFF0000u), inv));
+            *reinterpret_cast<uint2 *>(codes + base + e0) = out;
+        }
     }
 }
 
@@ -1056,10 +1182,11 @@ int device_setup(int *sms_out) {
         if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
         // the warpgroup register split must fit in what a CTA is launched with;
         // otherwise setmaxnreg.inc would wait for registers that never come
-        const void *kernels[4] = {reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, false>),
-                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, false>),
-                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, true>),
-                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, true>)};
+        const void *kernels[5] = {reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, false, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, false, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<64, true, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, true, false>),
+                                  reinterpret_cast<const void *>(attn::attn_fwd_kernel<128, false, true>)};
         for (const void *kfn : kernels) {
             cudaFuncAttributes fa;
             if ((e = cudaFuncGetAttributes(&fa, kfn)) != cudaSuccess) return cuda_fail(e);
@@ -1067,18 +1194,21 @@ int device_setup(int *sms_out) {
                 2 * 128 * attn::SOFTMAX_REGS + 128 * attn::PRODUCER_REGS)
                 return ATTN_ERR_UNSUPPORTED;
         }
-        if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, false>,
+        if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, false, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false>,
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<128>::SMEM_ALLOC)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true>,
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true>,
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      Cfg<128>::SMEM_ALLOC)) != cudaSuccess)
+                                      Cfg<128>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Cfg<128, true>::SMEM_ALLOC)) != cudaSuccess)
             return cuda_fail(e);
         di.sms = sms;
         di.ready = true;
@@ -1106,6 +1236,20 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
         misaligned(lse, 4))
         return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
+int encode_map_u8(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int N, long long BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                             static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d)};
+    cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(attn::BM), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
     return ATTN_OK;
 }
 
@@ -1164,8 +1308,60 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, con
     p.div_splits = attn::make_fastdiv(1u);
     p.div_nq = attn::make_fastdiv(1u);
     p.o_part = p.lse_part = nullptr;
+    p.q_scale = p.k_scale = p.v_scale = nullptr;
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    attn::attn_fwd_kernel<D, false, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+// e4m3 operands with block scales (d = 128, plain forward)
+int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, const float *ks,
+               const float *vs, void *o, float *lse, int B, int Hq, int Hkv, int N, int causal, int window,
+               float scale, cudaStream_t stream, int sms) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    CUtensorMap mq, mk, mv, mo;
+    int rc;
+    if ((rc = encode_map_u8(enc, &mq, q8, 128, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
+    if ((rc = encode_map_u8(enc, &mk, k8, 128, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map_u8(enc, &mv, v8, 128, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mo, o, 128, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
+    attn::Params p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.key_len = nullptr;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.N = N;
+    p.group = Hq / Hkv;
+    p.causal = causal;
+    p.window = window >= N ? 0 : window;
+    p.sym = (p.window > 0 && !causal) ? 1 : 0;
+    p.n_kv = (N + attn::BN - 1) / attn::BN;
+    p.n_pairs = (p.n_kv + 1) / 2;
+    p.num_units = B * Hq * p.n_pairs;
+    p.sl2 = scale * 1.4426950408889634f;
+    p.timeout_ns = attn::WAIT_LIMIT_NS;
+    p.div_bh = attn::make_fastdiv(static_cast<uint32_t>(B * Hq));
+    p.div_hq = attn::make_fastdiv(static_cast<uint32_t>(Hq));
+    p.div_group = attn::make_fastdiv(static_cast<uint32_t>(p.group));
+    p.Nk = N;
+    p.pos_off = 0;
+    p.Nq = N;
+    p.splits = 1;
+    p.split_lo = p.split_len = p.split_hi = 0;
+    p.div_splits = attn::make_fastdiv(1u);
+    p.div_nq = attn::make_fastdiv(1u);
+    p.o_part = p.lse_part = nullptr;
+    p.q_scale = qs;
+    p.k_scale = ks;
+    p.v_scale = vs;
+    const int grid = p.num_units < sms ? p.num_units : sms;
+    attn::attn_fwd_kernel<128, false, true><<<grid, attn::NUM_THREADS, Cfg<128, true>::SMEM_ALLOC, stream>>>(
+        mq, mk, mv, mo, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
@@ -1285,6 +1481,7 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
     p.div_splits = attn::make_fastdiv(static_cast<uint32_t>(splits));
     p.div_nq = attn::make_fastdiv(static_cast<uint32_t>(Nq));
     p.num_units = static_cast<int>(bhkv * splits);
+    p.q_scale = p.k_scale = p.v_scale = nullptr;
     if (splits > 1) {
         p.o_part = static_cast<float *>(workspace);
         const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * D * sizeof(float);
@@ -1293,7 +1490,7 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
         p.o_part = p.lse_part = nullptr;
     }
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, true><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     if (splits > 1) {
@@ -1386,6 +1583,40 @@ int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o
                                  scratch, attn::NOALLOC_SCRATCH_BYTES, s, sms);
     return launch_decode<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, causal, window, scale, splits,
                               scratch, attn::NOALLOC_SCRATCH_BYTES, s, sms);
+}
+
+int attn_quantize_e4m3(const void *x, void *codes, float *scales, int BH, int N, int d, void *stream) {
+    if (!x || !codes || !scales) return ATTN_ERR_NULLPTR;
+    if (BH < 1 || N < 1 || N > (1 << 30)) return ATTN_ERR_SHAPE;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (misaligned(x, 16) || misaligned(codes, 8) || misaligned(scales, 4)) return ATTN_ERR_ALIGN;
+    const int nblk = (N + attn::BM - 1) / attn::BM;
+    if (static_cast<long long>(BH) > 65535) return ATTN_ERR_SHAPE;  // grid y
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(BH));
+    if (d == 128)
+        attn::quantize_e4m3_kernel<128><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                              static_cast<uint8_t *>(codes), scales, N, nblk);
+    else
+        attn::quantize_e4m3_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                             static_cast<uint8_t *>(codes), scales, N, nblk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_scale, const float *k_scale,
+                 const float *v_scale, void *o, float *lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                 int window, float scale, void *stream) {
+    if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_NULLPTR;
+    int rc = validate(q8, k8, v8, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (misaligned(q_scale, 4) || misaligned(k_scale, 4) || misaligned(v_scale, 4)) return ATTN_ERR_ALIGN;
+    int sms = 0;
+    if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
+    return launch_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, N, causal, window, scale,
+                      static_cast<cudaStream_t>(stream), sms);
 }
 
 int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse, void *dq,

@@ -152,6 +152,29 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// the same two forms with e4m3 operands (kind::f8f6f4, K = 32 per instruction)
+__device__ __forceinline__ void mma_ss_elect_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_elect_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -248,6 +271,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -289,6 +319,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0), fp32 accumulator;
+// the same bit layout as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------------------ scalar helpers
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -322,6 +359,38 @@ __device__ __forceinline__ void add_bf16x2_halves(float &acc_lo, float &acc_hi, 
         "add.rn.f32.bf16 %1, h, %1;\n\t}"
         : "+f"(acc_lo), "+f"(acc_hi)
         : "r"(packed));
+}
+
+// four floats -> four e4m3 codes (round to nearest even, saturating at 448), x0 in the
+// lowest byte
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// acc_a += value of the low two e4m3 codes of `w`, acc_b += the high two (each code
+// widened exactly, through f16)
+__device__ __forceinline__ void add_e4m3x4(float &acc_a, float &acc_b, uint32_t w) {
+    asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 fl, fh;\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 fl, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 fh, h;\n\t"
+        "mov.b32 {a0, a1}, fl;\n\t"
+        "mov.b32 {b0, b1}, fh;\n\t"
+        "add.rn.f32.f16 %0, a0, %0;\n\t"
+        "add.rn.f32.f16 %0, a1, %0;\n\t"
+        "add.rn.f32.f16 %1, b0, %1;\n\t"
+        "add.rn.f32.f16 %1, b1, %1;\n\t}"
+        : "+f"(acc_a), "+f"(acc_b)
+        : "r"(w));
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // two floats -> packed bf16x2 (round to nearest even), `lo` in the low half

@@ -140,6 +140,42 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_quantize_e4m3 -- FP8 block quantisation, as the FlashAttention-3 review's "Block
+ * Quantization" describes it (deepmi.me): Q, K and V are split into blocks of B_r = 128
+ * rows x d, each block gets its own scale from its largest magnitude, and the scaled
+ * values are rounded to FP8 e4m3 (4-bit exponent, 3-bit mantissa; the variant with no
+ * infinity, largest value 448).
+ *
+ *   x       device, bf16 [BH, N, d] (any leading shape flattened to BH heads), 16-byte
+ *           aligned (read); d is 64 or 128
+ *   codes   device, uint8 [BH, N, d], 8-byte aligned (written): e4m3(x * 448 / amax),
+ *           round to nearest even, saturating at 448
+ *   scales  device, fp32 [BH, ceil(N / 128)], 4-byte aligned (written): amax / 448 of
+ *           each block (1 for an all-zero block); the value of a code is code x scale
+ * The division 448 / amax and the products are IEEE fp32 operations. BH <= 65535.
+ */
+int attn_quantize_e4m3(const void *x, void *codes, float *scales, int BH, int N, int d, void *stream);
+
+/*
+ * attn_fwd_fp8 -- the attention forward of attn_fwd on e4m3 operands (the FP8 path of the
+ * FlashAttention-3 review): Q, K, V given as codes and block scales from
+ * attn_quantize_e4m3; the computed result is attention on the dequantised values.
+ *
+ *   q8       device, uint8 [B, Hq, N, d] e4m3 codes; k8, v8 [B, Hkv, N, d]; 16-byte aligned
+ *   q_scale  device, fp32 [B * Hq, ceil(N / 128)]; k_scale, v_scale [B * Hkv, ceil(N / 128)]
+ *   o, lse, B, Hq, Hkv, N, causal, window, scale, stream   as for attn_fwd
+ *   d        128 (ATTN_ERR_UNSUPPORTED otherwise)
+ *
+ * S = q_scale x k_scale x (Q8 K8^T) exactly (fp32 accumulation); P is rounded to e4m3 for
+ * the P.V product, with each V block's scale folded into P relative to the head's
+ * largest V scale; O is normalised by the sum of the P values actually used, the LSE by
+ * the unrounded sum.
+ */
+int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_scale,
+                 const float *k_scale, const float *v_scale, void *o, float *lse, int B, int Hq,
+                 int Hkv, int N, int d, int causal, int window, float scale, void *stream);
+
+/*
  * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that cannot allocate device
  * memory. The pages have no counterpart to this entry point; it exists for users of the
  * library.

@@ -20,6 +20,7 @@ def test_exports_every_declared_symbol(lib):
     names = ea.header_functions()
     assert set(names) >= {"attn_fwd", "attn_fwd_padded", "attn_fwd_decode",
                           "attn_fwd_decode_workspace_size", "attn_fwd_decode_noalloc",
+                          "attn_quantize_e4m3", "attn_fwd_fp8",
                           "attn_fwd_host", "attn_status_str",
                           "attn_last_cuda_error",
                           "attn_device_error", "attn_selftest_wait_timeout", "attn_version"}
@@ -109,6 +110,21 @@ def test_decode_workspace_size(lib):
     assert lib.attn_fwd_decode_workspace_size(1, 4, 1, 1, 1000, 64, 50) == \
         lib.attn_fwd_decode_workspace_size(1, 4, 1, 1, 1000, 64, 8)
     assert lib.attn_fwd_decode_workspace_size(1, 4, 3, 1, 100, 64, 2) == 0   # bad shape
+
+
+def test_fp8_entries_validate(lib):
+    assert lib.attn_quantize_e4m3(None, A, A, 1, 128, 128, None) == ea.ATTN_ERR_NULLPTR
+    assert lib.attn_quantize_e4m3(A, A, A, 1, 128, 96, None) == ea.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_quantize_e4m3(A, A + 4, A, 1, 128, 128, None) == ea.ATTN_ERR_ALIGN
+    assert lib.attn_quantize_e4m3(A, A, A, 70000, 128, 128, None) == ea.ATTN_ERR_SHAPE
+    args = [A, A, A, A, A, A, A, A, 1, 1, 1, 128]
+    assert lib.attn_fwd_fp8(*args, 64, 0, 0, 0.1, None) == ea.ATTN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[3] = None
+    assert lib.attn_fwd_fp8(*bad, 128, 0, 0, 0.1, None) == ea.ATTN_ERR_NULLPTR
+    bad = list(args)
+    bad[4] = A + 2
+    assert lib.attn_fwd_fp8(*bad, 128, 0, 0, 0.1, None) == ea.ATTN_ERR_ALIGN
 
 
 def test_host_entry_validates_both_buffer_sets(lib):

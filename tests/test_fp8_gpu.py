@@ -1,0 +1,81 @@
+"""The FP8 (e4m3) path through the C ABI: block quantisation must match the oracle's
+bit for bit (integer codes and fp32 scales), and attention on the e4m3 operands is
+compared with the fp64 oracle on the dequantised values.
+
+Tolerance of the FP8 attention (from the arithmetic): S is exact up to fp32
+accumulation, so the LSE keeps the 1e-3 relative bar. P is rounded to e4m3 (3 mantissa
+bits: relative error delta <= 2^-4) for the P.V product and O is normalised by the
+rounded weights, so O - O_ref = sum_j w_j (delta_j - mean delta) (v_j - O_ref) / (1 +
+mean delta); per element that is at most 2 * 2^-4 * 2 max|v| / (1 - 2^-4), and its root
+mean square is bounded by 2^-4 * RMS(v).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_self_attention_fwd_b300 as ea
+from exact_self_attention_fwd_b300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+MAX_FRAC = 2 * 2.0 ** -4 * 2 / (1 - 2.0 ** -4)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 128, 128), (2, 3, 300, 128), (1, 4, 1000, 64), (2, 1, 77, 64)])
+def test_quantize_matches_oracle_bit_for_bit(shape):
+    g = torch.Generator().manual_seed(sum(shape))
+    x = (torch.randn(shape, generator=g) * torch.exp(2 * torch.randn(shape[:-1] + (1,), generator=g))).bfloat16()
+    x[..., 0, 0] = 0.0
+    codes, scales = ea.quantize_e4m3(x.to(DEV))
+    torch.cuda.synchronize()
+    c_ref, s_ref = oracle.quantize_e4m3_blocks(x, rows=128)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(scales.cpu().numpy().reshape(s_ref.shape), s_ref)
+
+
+def test_quantize_zero_block():
+    x = torch.zeros(1, 256, 128, dtype=torch.bfloat16, device=DEV)
+    x[0, 200, 3] = 2.0
+    codes, scales = ea.quantize_e4m3(x)
+    torch.cuda.synchronize()
+    assert scales[0, 0].item() == 1.0 and codes[0, :128].eq(0).all()
+    assert scales[0, 1].item() == np.float32(2.0) / np.float32(448.0)
+
+
+def run_fp8(B, Hq, Hkv, N, causal, window, seed):
+    d = 128
+    q, k, v = make_qkv(B, Hq, Hkv, N, d, seed)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    (q8, qs), (k8, ks), (v8, vs) = ea.quantize_e4m3(qd), ea.quantize_e4m3(kd), ea.quantize_e4m3(vd)
+    scale = 1.0 / math.sqrt(d)
+    out, lse = ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal, window=window, scale=scale)
+    torch.cuda.synchronize()
+    assert ea.device_error() == ea.ATTN_OK
+    deq = [oracle.dequantize_e4m3_blocks(c.cpu().numpy(), s.cpu().numpy()) for c, s in
+           ((q8, qs), (k8, ks), (v8, vs))]
+    o_ref, l_ref = oracle.attn_ref_f64in(deq[0], deq[1], deq[2], causal, window, scale)
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    assert np.isfinite(o).all() and np.isfinite(l).all()
+    lerr = np.abs(l - l_ref) / np.maximum(1.0, np.abs(l_ref))
+    assert lerr.max() <= 1e-3, f"LSE rel err {lerr.max():.3g}"
+    vmax = np.abs(deq[2]).max()
+    err = np.abs(o - o_ref)
+    assert err.max() <= MAX_FRAC * vmax + 2.0 ** -6, f"max |dO| {err.max():.3g}"
+    rmse = float(np.sqrt(np.mean(err ** 2)))
+    assert rmse <= 2.0 ** -4 * float(np.sqrt(np.mean(deq[2] ** 2))), f"RMSE {rmse:.3g}"
+    return err.max(), rmse
+
+
+@pytest.mark.parametrize("N", [128, 129, 300, 1000])
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 200), (False, 150)])
+def test_fp8_attention_vs_oracle(N, causal, window):
+    mx, rmse = run_fp8(2, 4, 2, N, causal, window, seed=6000 + N + window)
+    print(N, causal, window, mx, rmse)
+
+
+def test_fp8_many_units():
+    run_fp8(2, 32, 8, 2048, True, 0, seed=6100)
