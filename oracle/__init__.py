@@ -14,6 +14,9 @@ Parity status of each function (see the pins in ``tests/test_oracle_pins.py`` an
   an independent library routine, and mutation tests).
   attn_ref_decode -- pinned (the last rows of the plain forward, a zero-query closed
   form, brute force and torch SDPA with an offset mask).
+  attn_ref_bwd -- pinned (torch autograd through fp64 scaled_dot_product_attention with
+  the same masks, central finite differences of the oracle's own forward, and the
+  invariants sum_j ds_ij = 0 and dv = sum of p^T do).
   e4m3_encode / e4m3_decode / quantize_e4m3_blocks / attn_ref_fp8 -- pinned (every code
   against torch's float8_e4m3fn, the rounding of every bf16 value in range, block
   reconstruction bounds, exactness on representable inputs, and the block-vs-tensor
@@ -76,6 +79,9 @@ def _declare(lib):
     lib.attn_ref_quantize_e4m3_blocks.argtypes = [u16p, i64, i64, i64, i64, u8p,
                                                   ctypes.POINTER(ctypes.c_float)]
     lib.attn_ref_quantize_e4m3_blocks.restype = ctypes.c_int
+    lib.attn_ref_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
+                                     ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p]
+    lib.attn_ref_bwd_f64.restype = ctypes.c_int
     return lib
 
 
@@ -284,3 +290,28 @@ def attn_ref_fp8(q, k, v, causal: bool = False, window: int = 0, scale: float | 
             deq.append(dequantize_e4m3_blocks(codes, sc, rows=block_rows))
     o, lse = attn_ref_f64in(deq[0], deq[1], deq[2], causal, window, scale, rows)
     return o, lse, deq
+
+
+def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: float | None = None,
+                 key_len=None, lib=None):
+    """fp64 gradients (dq [B,Hq,N,d], dk, dv [B,Hkv,N,d]) of the forward's o for the
+    upstream gradient do [B,Hq,N,d] (all inputs bf16)."""
+    qb, kb, vb, db = (_as_bits(t) for t in (q, k, v, do))
+    B, Hq, N, d = qb.shape
+    Hkv = kb.shape[1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    dq = np.empty((B, Hq, N, d), dtype=np.float64)
+    dk = np.empty((B, Hkv, N, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, N, d), dtype=np.float64)
+    kl = None if key_len is None else np.ascontiguousarray(np.asarray(key_len, dtype=np.int32))
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = (lib or load()).attn_ref_bwd_f64(
+        qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
+        B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+        kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
+        dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return dq, dk, dv

@@ -355,3 +355,96 @@ int attn_ref_quantize_e4m3_blocks(const uint16_t *x, int64_t BH, int64_t N, int6
     }
     return 0;
 }
+
+/*
+ * Backward pass: gradients of the attention forward (o above) with respect to q, k, v
+ * for an upstream gradient do_ = dL/do, restated from the chain rule through the
+ * definition (the pages only say that the backward pass exists and costs about 2.5x the
+ * forward, FlashAttention-3 review, FLOPs answer):
+ *
+ *   p_ij  = exp(s_ij - lse_i) for j in J(i), 0 otherwise       (the softmax weights)
+ *   dp_ij = do_i . v_j                                          (dL/dp)
+ *   ds_ij = p_ij (dp_ij - sum_l p_il dp_il)                     (through the softmax)
+ *   dq_i  = scale sum_j ds_ij k_j
+ *   dk_j  = scale sum over (query head of the group, i) of ds_ij q_i
+ *   dv_j  = sum over (query head of the group, i) of p_ij do_i
+ *
+ * Inputs bf16 bits (q, k, v, do_ as for the forward); outputs fp64, dq [B,Hq,N,d], dk and
+ * dv [B,Hkv,N,d]. Single-threaded over heads (test sizes only).
+ */
+int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int causal,
+                     int64_t window, double scale, const int32_t *key_len,
+                     double *dq, double *dk, double *dv) {
+    if (!q || !k || !v || !do_ || !dq || !dk || !dv) return -1;
+    int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc) return rc;
+    const int64_t group = Hq / Hkv;
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!p || !dp) {
+        free(p);
+        free(dp);
+        return -5;
+    }
+    for (int64_t i = 0; i < B * Hq * N * d; ++i) dq[i] = 0.0;
+    for (int64_t i = 0; i < B * Hkv * N * d; ++i) dk[i] = dv[i] = 0.0;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t L = key_len ? (int64_t)key_len[b] : N;
+        if (L < 0) L = 0;
+        if (L > N) L = N;
+        for (int64_t hq = 0; hq < Hq; ++hq) {
+            const int64_t kv = hq / group;
+            const uint16_t *qh = q + (b * Hq + hq) * N * d, *doh = do_ + (b * Hq + hq) * N * d;
+            const uint16_t *kh = k + (b * Hkv + kv) * N * d, *vh = v + (b * Hkv + kv) * N * d;
+            double *dqh = dq + (b * Hq + hq) * N * d;
+            double *dkh = dk + (b * Hkv + kv) * N * d, *dvh = dv + (b * Hkv + kv) * N * d;
+            for (int64_t i = 0; i < N; ++i) {
+                /* scores, their maximum and the log-sum-exp over the visible keys */
+                double m = -INFINITY;
+                int64_t nvis = 0;
+                for (int64_t j = 0; j < N; ++j) {
+                    p[j] = 0.0;
+                    if (!key_visible(i, j, causal, window, L)) continue;
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += bf16_bits_to_double(qh[i * d + c]) * bf16_bits_to_double(kh[j * d + c]);
+                    p[j] = scale * dot; /* the score, for now */
+                    if (p[j] > m) m = p[j];
+                    ++nvis;
+                }
+                if (nvis == 0) continue; /* a row with no visible key contributes nothing */
+                double l = 0.0;
+                for (int64_t j = 0; j < N; ++j)
+                    if (key_visible(i, j, causal, window, L)) l += exp(p[j] - m);
+                const double lse = m + log(l);
+                double pdp = 0.0;
+                for (int64_t j = 0; j < N; ++j) {
+                    if (!key_visible(i, j, causal, window, L)) {
+                        p[j] = 0.0;
+                        dp[j] = 0.0;
+                        continue;
+                    }
+                    p[j] = exp(p[j] - lse);
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += bf16_bits_to_double(doh[i * d + c]) * bf16_bits_to_double(vh[j * d + c]);
+                    dp[j] = dot;
+                    pdp += p[j] * dp[j];
+                }
+                for (int64_t j = 0; j < N; ++j) {
+                    if (p[j] == 0.0 && dp[j] == 0.0) continue;
+                    const double ds = p[j] * (dp[j] - pdp);
+                    for (int64_t c = 0; c < d; ++c) {
+                        dqh[i * d + c] += scale * ds * bf16_bits_to_double(kh[j * d + c]);
+                        dkh[j * d + c] += scale * ds * bf16_bits_to_double(qh[i * d + c]);
+                        dvh[j * d + c] += p[j] * bf16_bits_to_double(doh[i * d + c]);
+                    }
+                }
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    return 0;
+}
