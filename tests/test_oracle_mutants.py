@@ -19,9 +19,10 @@ MUTANTS = {
     "window_off_by_one": ("if (window > 0 && i - j >= window) return 0;",
                           "if (window > 0 && i - j > window) return 0;"),
     # wrong head map for grouped-query attention
-    "gqa_modulo_map": ("const int64_t kv = hq / group;", "const int64_t kv = hq % jb->Hkv;"),
+    "gqa_modulo_map": ("const int64_t group = jb->Hq / jb->Hkv;\n    const int64_t kv = hq / group;",
+                       "const int64_t group = jb->Hq / jb->Hkv;\n    const int64_t kv = hq % jb->Hkv;"),
     # a dropped term in the log-sum-exp
-    "lse_drops_max": ("const double lse = m + log(l);", "const double lse = log(l);"),
+    "lse_drops_max": ("    }\n    const double lse = m + log(l);", "    }\n    const double lse = log(l);"),
     # transposed operands: the score uses V rows instead of K rows
     "scores_from_v": ("dot += qd[c] * KVAL(j, c);", "dot += qd[c] * VVAL(j, c);"),
     # a wrong sign in the probability
