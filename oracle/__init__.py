@@ -82,6 +82,10 @@ def _declare(lib):
     lib.attn_ref_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                      ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p]
     lib.attn_ref_bwd_f64.restype = ctypes.c_int
+    lib.attn_ref_bwd_given_o_f64.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                             i64, ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p,
+                                             f64p]
+    lib.attn_ref_bwd_given_o_f64.restype = ctypes.c_int
     return lib
 
 
@@ -293,9 +297,13 @@ def attn_ref_fp8(q, k, v, causal: bool = False, window: int = 0, scale: float | 
 
 
 def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: float | None = None,
-                 key_len=None, lib=None):
+                 key_len=None, lib=None, o=None):
     """fp64 gradients (dq [B,Hq,N,d], dk, dv [B,Hkv,N,d]) of the forward's o for the
-    upstream gradient do [B,Hq,N,d] (all inputs bf16)."""
+    upstream gradient do [B,Hq,N,d] (all inputs bf16).
+
+    o: None, or a given forward output [B,Hq,N,d] (any float type, taken as fp64): the
+    softmax row sum of dp is then formed as do_i . o_i from it, as a backward pass that
+    takes the forward's output as an input does (identical for the exact output)."""
     qb, kb, vb, db = (_as_bits(t) for t in (q, k, v, do))
     B, Hq, N, d = qb.shape
     Hkv = kb.shape[1]
@@ -307,7 +315,19 @@ def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: floa
     kl = None if key_len is None else np.ascontiguousarray(np.asarray(key_len, dtype=np.int32))
     u16p = ctypes.POINTER(ctypes.c_uint16)
     f64p = ctypes.POINTER(ctypes.c_double)
-    rc = (lib or load()).attn_ref_bwd_f64(
+    L = lib or load()
+    if o is not None:
+        ob = np.ascontiguousarray(np.asarray(o.double().numpy() if hasattr(o, "double") else o,
+                                             dtype=np.float64).reshape(B, Hq, N, d))
+        rc = L.attn_ref_bwd_given_o_f64(
+            qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
+            ob.ctypes.data_as(f64p), B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+            kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
+            dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (code {rc})")
+        return dq, dk, dv
+    rc = L.attn_ref_bwd_f64(
         qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
         B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
         kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,

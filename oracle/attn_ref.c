@@ -371,11 +371,17 @@ int attn_ref_quantize_e4m3_blocks(const uint16_t *x, int64_t BH, int64_t N, int6
  *
  * Inputs bf16 bits (q, k, v, do_ as for the forward); outputs fp64, dq [B,Hq,N,d], dk and
  * dv [B,Hkv,N,d]. Single-threaded over heads (test sizes only).
+ *
+ * o_in: NULL, or a given forward output [B,Hq,N,d] (fp64). A backward pass that takes
+ * the forward's output as an input forms the row sum sum_l p_il dp_il as do_i . o_i,
+ * which equals it exactly when o_i is the exact output (o_i = sum_l p_il v_l); with a
+ * given o_in the row sum is do_i . o_in_i, so the gradients are those a backward pass
+ * computes from that o.
  */
-int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
-                     int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int causal,
-                     int64_t window, double scale, const int32_t *key_len,
-                     double *dq, double *dk, double *dv) {
+static int bwd_core(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                    const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                    int causal, int64_t window, double scale, const int32_t *key_len,
+                    double *dq, double *dk, double *dv) {
     if (!q || !k || !v || !do_ || !dq || !dk || !dv) return -1;
     int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
     if (rc) return rc;
@@ -432,6 +438,11 @@ int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
                     dp[j] = dot;
                     pdp += p[j] * dp[j];
                 }
+                if (o_in) {
+                    const double *oi = o_in + ((b * Hq + hq) * N + i) * d;
+                    pdp = 0.0;
+                    for (int64_t c = 0; c < d; ++c) pdp += bf16_bits_to_double(doh[i * d + c]) * oi[c];
+                }
                 for (int64_t j = 0; j < N; ++j) {
                     if (p[j] == 0.0 && dp[j] == 0.0) continue;
                     const double ds = p[j] * (dp[j] - pdp);
@@ -447,4 +458,19 @@ int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
     free(p);
     free(dp);
     return 0;
+}
+
+int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int causal,
+                     int64_t window, double scale, const int32_t *key_len,
+                     double *dq, double *dk, double *dv) {
+    return bwd_core(q, k, v, do_, NULL, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv);
+}
+
+int attn_ref_bwd_given_o_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                             const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                             int causal, int64_t window, double scale, const int32_t *key_len,
+                             double *dq, double *dk, double *dv) {
+    if (!o_in) return -1;
+    return bwd_core(q, k, v, do_, o_in, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv);
 }

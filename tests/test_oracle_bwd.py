@@ -118,6 +118,76 @@ def test_bwd_invariants():
     assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
 
 
+def test_bwd_given_exact_o_equals_chain_rule():
+    # do_i . o_i equals sum_j p_ij dp_ij when o is the exact output
+    g = torch.Generator().manual_seed(58)
+    B, Hq, Hkv, N, d = 2, 4, 2, 37, 16
+    q = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    k, v = (torch.randn(B, Hkv, N, d, generator=g).bfloat16() for _ in range(2))
+    do = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    for causal, W, kl in ((True, 0, None), (False, 5, [37, 11]), (True, 9, [20, 37])):
+        o, _ = oracle.attn_ref(q, k, v, causal=causal, window=W, scale=0.3, key_len=kl)
+        a = oracle.attn_ref_bwd(q, k, v, do, causal=causal, window=W, scale=0.3, key_len=kl)
+        b = oracle.attn_ref_bwd(q, k, v, do, causal=causal, window=W, scale=0.3, key_len=kl, o=o)
+        for x, y in zip(a, b):
+            np.testing.assert_allclose(y, x, atol=1e-11, rtol=0)
+
+
+def _linear_response_error(lib=None):
+    """Largest deviation from the closed-form response of the given-o gradients to a
+    change of one element of o: moving o_ic by eps shifts the row sum by eps do_ic,
+    hence ds_ij by -p_ij eps do_ic. dq_i moves by -scale eps do_ic sum_j p_ij k_j (the
+    forward with k in place of v), dk_j by -scale eps do_ic p_ij q_i (p_ij by brute
+    force), every other dq row and all of dv stay."""
+    g = torch.Generator().manual_seed(59)
+    B, Hq, Hkv, N, d = 1, 2, 1, 23, 8
+    q = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    k, v = (torch.randn(B, Hkv, N, d, generator=g).bfloat16() for _ in range(2))
+    do = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    scale, eps, (hq, i, c) = 0.4, 1e-3, (1, 9, 5)
+    o, _ = oracle.attn_ref(q, k, v, causal=True, scale=scale)
+    o2 = o.copy()
+    o2[0, hq, i, c] += eps
+    dq1, dk1, dv1 = oracle.attn_ref_bwd(q, k, v, do, causal=True, scale=scale, o=o, lib=lib)
+    dq2, dk2, dv2 = oracle.attn_ref_bwd(q, k, v, do, causal=True, scale=scale, o=o2, lib=lib)
+    pk, _ = oracle.attn_ref(q, k, k, causal=True, scale=scale)
+    want = np.zeros_like(dq1)
+    want[0, hq, i] = -scale * eps * float(do[0, hq, i, c]) * pk[0, hq, i]
+    s = scale * (q[0, hq, i].double() @ k[0, 0].double().T).numpy()
+    s[i + 1:] = -np.inf
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    want_k = -scale * eps * float(do[0, hq, i, c]) * p[:, None] * q[0, hq, i].double().numpy()[None, :]
+    return max(np.abs(dq2 - dq1 - want).max(), np.abs(dv2 - dv1).max(), np.abs(dk2 - dk1 - want_k[None, None]).max())
+
+
+def test_bwd_given_o_linear_response():
+    assert _linear_response_error() <= 1e-12
+
+
+GIVEN_O_MUTANTS = {
+    # a given output is ignored (the row sum stays the exact one)
+    "given_o_ignored": ("for (int64_t c = 0; c < d; ++c) pdp += bf16_bits_to_double(doh[i * d + c]) * oi[c];",
+                        "for (int64_t c = 0; c < d; ++c) pdp += p[0] * 0.0 * oi[c];"),
+    # a given output read from the wrong row
+    "given_o_wrong_row": ("const double *oi = o_in + ((b * Hq + hq) * N + i) * d;",
+                          "const double *oi = o_in + ((b * Hq + hq) * N + i / 2) * d;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GIVEN_O_MUTANTS))
+def test_given_o_pin_catches_mutant(name, tmp_path):
+    with open(oracle._SRC) as f:
+        src = f.read()
+    old, new = GIVEN_O_MUTANTS[name]
+    assert src.count(old) == 1
+    mutated = tmp_path / "attn_ref_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = str(tmp_path / "libattn_ref_mutant.so")
+    oracle.build(force=True, src=str(mutated), out=so)
+    assert _linear_response_error(oracle.load(so)) > 1e-9, f"mutant {name} not caught"
+
+
 BWD_MUTANTS = {
     # the softmax gradient without its row term
     "ds_without_row_term": ("const double ds = p[j] * (dp[j] - pdp);", "const double ds = p[j] * dp[j];"),
