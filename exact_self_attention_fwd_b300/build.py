@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn_fwd.so")
 SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(INCLUDE, "attn_api.h")]
+DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "attn_bwd.cuh"),
+                  os.path.join(INCLUDE, "attn_api.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -56,7 +57,13 @@ def check_registers(ptxas_log: str) -> None:
     blocks = re.split(r"Compiling entry function", ptxas_log)
     seen = 0
     for blk in blocks[1:]:
-        if "attn_fwd_kernel" not in blk.split("\n", 1)[0]:
+        head = blk.split("\n", 1)[0]
+        if "attn_bwd_kernel" in head:
+            spill = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", blk)
+            if spill and (int(spill.group(1)) or int(spill.group(2))):
+                raise RuntimeError("backward kernel spills registers:\n" + blk)
+            continue
+        if "attn_fwd_kernel" not in head:
             continue
         seen += 1
         regs = int(re.search(r"Used (\d+) registers", blk).group(1))

@@ -1,0 +1,504 @@
+// Backward pass of the exact attention forward, on the tensor cores (sm_103a). Included
+// into attn_fwd.cu inside namespace attn, so it shares the device status word, the
+// bounded waits and the inline-PTX wrappers.
+//
+// Gradients, for the upstream gradient dO of O (the chain rule through the definition):
+//   P  = exp(scale S - lse)            (the forward's softmax weights; 0 where masked)
+//   dP = dO V^T,  D_i = dO_i . O_i     (D_i = sum_j P_ij dP_ij, since O_i = sum_j P_ij V_j)
+//   dS = P o (dP - D)
+//   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO   (dK, dV summed over a group's heads)
+//
+// Three kernels:
+//   bwd_preprocess_kernel  D = rowsum(dO o O) in fp32 (one warp per row)
+//   bwd kernel, MODE 0     key-stationary: a CTA holds K_j, V_j of one key tile and
+//                          streams (Q_i, dO_i) over every query head of the group and
+//                          every query tile that sees the keys: S^T = K Q^T and
+//                          dP^T = V dO^T into tensor memory, P^T and dS^T by the compute
+//                          warps, then dV += P^T dO and dK += dS^T Q accumulate in tensor
+//                          memory across the whole stream
+//   bwd kernel, MODE 1     query-stationary: holds Q_i, dO_i and streams (K_j, V_j):
+//                          S = Q K^T, dP = dO V^T, dS, then dQ += dS K (no atomics)
+// Warps: 0-3 compute (one tensor-memory row each thread), 4 TMA producer, 5 MMA issuer,
+// 6-7 idle. Tensor memory: S (or S^T) [0,128), dP [128,256), two accumulators from 256.
+#pragma once
+
+constexpr int BWD_THREADS = 256;
+constexpr int BWD_WARP_TMA = 4;
+constexpr int BWD_WARP_MMA = 5;
+
+struct BwdParams {
+    const float *dsum;              // D = dO . O per query row, fp32 [B * Hq * N]
+    const float *lse;               // forward LSE, natural log, [B * Hq * N]
+    __nv_bfloat16 *dq, *dk, *dv;
+    const int *key_len;
+    int B, Hq, Hkv, N, group;
+    int causal, window, sym;
+    int n_kv, num_units;
+    float sl2, scale;
+    unsigned long long timeout_ns;
+    FastDiv div_bhkv, div_hkv, div_bhq, div_hq, div_group;
+};
+
+template <int D>
+struct BwdCfg {
+    static constexpr int CHUNK_BYTES = BM * 128;  // 64 bf16 columns, 128-byte swizzled
+    static constexpr int NCHUNK = D / 64;
+    static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
+    static constexpr int STAGES = D == 64 ? 4 : 2;              // streamed tile pairs in flight
+    static constexpr int SMEM_FIX = 0;                          // the two stationary tiles
+    static constexpr int SMEM_RING = 2 * TILE_BYTES;            // STAGES x two streamed tiles
+    static constexpr int SMEM_VEC = SMEM_RING + STAGES * 2 * TILE_BYTES;  // per slot: lse2, D
+    static constexpr int SMEM_BAR = SMEM_VEC + STAGES * 2 * BM * 4;
+    static constexpr int B_FIXFULL = 0, B_FIXEMPTY = 1, B_FULL = 2, B_EMPTY = 2 + STAGES;
+    static constexpr int B_SDP = 2 + 2 * STAGES;  // S and dP computed
+    static constexpr int B_PDS = B_SDP + 1;       // P (MODE 0) and dS written (4 warps)
+    static constexpr int B_ACC = B_PDS + 1;       // accumulators of the unit complete
+    static constexpr int B_DRAIN = B_ACC + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_ALLOC = SMEM_CTL + 16 + 1024;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_A0 = 256, COL_A1 = 256 + D;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
+};
+
+// D_i = sum_c dO[i, c] O[i, c] in fp32, one warp per row
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                             const __nv_bfloat16 *__restrict__ dout,
+                                                             float *__restrict__ dsum, long long rows) {
+    constexpr int PER = D / 32;  // bf16 per lane
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16 *a = o + row * D + lane * PER;
+    const __nv_bfloat16 *b = dout + row * D + lane * PER;
+    float acc = 0.f;
+    if constexpr (PER == 4) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(a), y = *reinterpret_cast<const uint2 *>(b);
+        acc = fmaf(__uint_as_float(x.x << 16), __uint_as_float(y.x << 16), acc);
+        acc = fmaf(__uint_as_float(x.x & 0xFFFF0000u), __uint_as_float(y.x & 0xFFFF0000u), acc);
+        acc = fmaf(__uint_as_float(x.y << 16), __uint_as_float(y.y << 16), acc);
+        acc = fmaf(__uint_as_float(x.y & 0xFFFF0000u), __uint_as_float(y.y & 0xFFFF0000u), acc);
+    } else {
+        const uint32_t x = *reinterpret_cast<const uint32_t *>(a), y = *reinterpret_cast<const uint32_t *>(b);
+        acc = fmaf(__uint_as_float(x << 16), __uint_as_float(y << 16), acc);
+        acc = fmaf(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(y & 0xFFFF0000u), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dsum[row] = acc;
+}
+
+__device__ __forceinline__ int bwd_valid_len(const BwdParams &p, int b) {
+    if (!p.key_len) return p.N;
+    return min(max(__ldg(p.key_len + b), 0), p.N);
+}
+
+// Queries a key row k (of a batch with valid length L) is visible to: [qlo, qhi], empty
+// when qlo > qhi. (The transpose of the forward's key interval of a query row.)
+__device__ __forceinline__ void key_query_interval(const BwdParams &p, int k, int L, int &qlo, int &qhi) {
+    qlo = 0;
+    qhi = L - 1;
+    if (k >= L) {
+        qlo = 1;
+        qhi = 0;
+        return;
+    }
+    if (p.causal) qlo = k;
+    if (p.window > 0) {
+        qhi = min(qhi, k + p.window - 1);
+        if (p.sym) qlo = max(qlo, k - p.window + 1);
+    }
+}
+
+// Keys a query row q is visible to: [klo, khi] (as in the forward).
+__device__ __forceinline__ void query_key_interval(const BwdParams &p, int q, int L, int &klo, int &khi) {
+    klo = 0;
+    khi = L - 1;
+    if (q >= L) {
+        klo = 1;
+        khi = 0;
+        return;
+    }
+    if (p.causal) khi = min(khi, q);
+    if (p.sym) khi = min(khi, q + p.window - 1);
+    if (p.window > 0) klo = max(0, q - p.window + 1);
+}
+
+// What one unit covers. MODE 0: the key tile j of (b, hkv) and the range of query tiles
+// [lo, hi) every head of the group streams. MODE 1: the query tile i of (b, hq) and the
+// key tiles [lo, hi) it streams.
+struct BwdUnit {
+    int b, tile, zfix, zstream0, L, lo, hi, steps;
+};
+
+template <int MODE>
+__device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams &p) {
+    BwdUnit w;
+    if constexpr (MODE == 0) {
+        const int BHkv = p.B * p.Hkv;
+        const int pr = fdiv(u, p.div_bhkv);
+        const int bhkv = u - pr * BHkv;
+        w.b = fdiv(bhkv, p.div_hkv);
+        const int hkv = bhkv - w.b * p.Hkv;
+        // heaviest first: under the look-ahead mask key tile 0 is seen by every query tile
+        w.tile = pr;
+        w.zfix = bhkv;
+        w.zstream0 = w.b * p.Hq + hkv * p.group;  // first query head of the group
+        w.L = bwd_valid_len(p, w.b);
+        w.lo = w.hi = 0;
+        const int k0 = w.tile * BN;
+        if (k0 < w.L) {
+            int qlo0, qhi0, qlo1, qhi1;
+            key_query_interval(p, k0, w.L, qlo0, qhi0);
+            key_query_interval(p, min(w.L, k0 + BN) - 1, w.L, qlo1, qhi1);
+            const int qlo = qlo0, qhi = max(qhi0, qhi1);
+            if (qlo <= qhi) {
+                w.lo = qlo / BM;
+                w.hi = qhi / BM + 1;
+            }
+        }
+        w.steps = p.group * (w.hi - w.lo);
+    } else {
+        const int BHq = p.B * p.Hq;
+        const int pr = fdiv(u, p.div_bhq);
+        const int bh = u - pr * BHq;
+        w.b = fdiv(bh, p.div_hq);
+        const int hq = bh - w.b * p.Hq;
+        w.tile = p.n_kv - 1 - pr;  // heaviest first under the look-ahead mask
+        w.zfix = bh;
+        w.zstream0 = w.b * p.Hkv + fdiv(hq, p.div_group);
+        w.L = bwd_valid_len(p, w.b);
+        w.lo = w.hi = 0;
+        const int q0 = w.tile * BM;
+        if (q0 < w.L) {
+            int klo0, khi0, klo1, khi1;
+            query_key_interval(p, q0, w.L, klo0, khi0);
+            query_key_interval(p, min(w.L, q0 + BM) - 1, w.L, klo1, khi1);
+            const int klo = klo0, khi = max(khi0, khi1);
+            if (klo <= khi) {
+                w.lo = klo / BN;
+                w.hi = khi / BN + 1;
+            }
+        }
+        w.steps = w.hi - w.lo;
+    }
+    return w;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sb = raw + pad;
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem + C::SMEM_CTL);
+    auto bar = [&](int i) -> uint32_t { return sb + C::SMEM_BAR + 8u * static_cast<uint32_t>(i); };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(C::B_FIXFULL), 1);
+        ptx::mbar_init(bar(C::B_FIXEMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar(C::B_FULL + s), 1);
+            ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        ptx::mbar_init(bar(C::B_SDP), 1);
+        ptx::mbar_init(bar(C::B_PDS), 4);
+        ptx::mbar_init(bar(C::B_ACC), 1);
+        ptx::mbar_init(bar(C::B_DRAIN), 1);
+        ctl->abort = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == BWD_WARP_TMA && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_do);
+    }
+    if (warp == BWD_WARP_MMA) {
+        ptx::tmem_alloc(sb + C::SMEM_CTL, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile uint32_t *abort_flag = &ctl->abort;
+    const unsigned long long limit = p.timeout_ns;
+    // stationary tiles: MODE 0 holds (K, V), MODE 1 holds (Q, dO); the streamed pair is
+    // (Q, dO) or (K, V)
+    const CUtensorMap *fix0 = MODE == 0 ? &tm_k : &tm_q;
+    const CUtensorMap *fix1 = MODE == 0 ? &tm_v : &tm_do;
+    const CUtensorMap *str0 = MODE == 0 ? &tm_q : &tm_k;
+    const CUtensorMap *str1 = MODE == 0 ? &tm_do : &tm_v;
+
+    if (warp == BWD_WARP_TMA) {
+        // ================================================================ producer
+        uint32_t it = 0, fix_it = 0;
+        bool ok = true;
+        for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
+            const BwdUnit w = bwd_unit<MODE>(u, p);
+            if (w.steps == 0) continue;
+            ok = wait_warp(bar(C::B_FIXEMPTY), (fix_it & 1u) ^ 1u, abort_flag, limit);
+            ++fix_it;
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx_elect(bar(C::B_FIXFULL), 2 * C::TILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NCHUNK; ++c) {
+                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + c * C::CHUNK_BYTES, fix0, bar(C::B_FIXFULL), c * 64,
+                                       w.tile * BM, w.zfix);
+                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + C::TILE_BYTES + c * C::CHUNK_BYTES, fix1,
+                                       bar(C::B_FIXFULL), c * 64, w.tile * BM, w.zfix);
+            }
+            for (int s = 0; ok && s < w.steps; ++s) {
+                // MODE 0: step s = (head g of the group, query tile i); MODE 1: key tile
+                const int n_t = w.hi - w.lo;
+                const int g = MODE == 0 ? s / n_t : 0;
+                const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
+                const int zs = w.zstream0 + g;
+                const uint32_t slot = it % C::STAGES, ph = ((it / C::STAGES) & 1u) ^ 1u;
+                ok = wait_warp(bar(C::B_EMPTY + slot), ph, abort_flag, limit);
+                if (!ok) break;
+                ++it;
+                if constexpr (MODE == 0) {
+                    // the streamed query tile's lse (in log2 units) and D, one value per
+                    // column, staged beside the tiles for the compute warps
+                    float *vec = reinterpret_cast<float *>(smem + C::SMEM_VEC) + slot * 2 * BM;
+#pragma unroll
+                    for (int r = 0; r < BM / 32; ++r) {
+                        const int qq = t * BM + r * 32 + lane;
+                        const size_t idx = static_cast<size_t>(zs) * p.N + qq;
+                        vec[r * 32 + lane] = qq < p.N ? __ldg(p.lse + idx) * 1.4426950408889634f : 0.f;
+                        vec[BM + r * 32 + lane] = qq < p.N ? __ldg(p.dsum + idx) : 0.f;
+                    }
+                    __syncwarp();
+                }
+                ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES);
+                const uint32_t dst = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES;
+#pragma unroll
+                for (int c = 0; c < C::NCHUNK; ++c) {
+                    ptx::tma_load_3d_elect(dst + c * C::CHUNK_BYTES, str0, bar(C::B_FULL + slot), c * 64, t * BM, zs);
+                    ptx::tma_load_3d_elect(dst + C::TILE_BYTES + c * C::CHUNK_BYTES, str1, bar(C::B_FULL + slot),
+                                           c * 64, t * BM, zs);
+                }
+            }
+        }
+        if (!ok) {
+            for (uint32_t slot = 0; slot < static_cast<uint32_t>(C::STAGES); ++slot) {
+                if (it <= slot) continue;
+                const uint32_t last = (it - 1u - slot) / C::STAGES * C::STAGES + slot;
+                drain_wait(bar(C::B_FULL + slot), (last / C::STAGES) & 1u, 100000000ull);
+            }
+            if (fix_it) drain_wait(bar(C::B_FIXFULL), (fix_it - 1u) & 1u, 100000000ull);
+        }
+    } else if (warp == BWD_WARP_MMA) {
+        // ================================================================ MMA issuer
+        constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(BM, D, true);
+        uint32_t it = 0, fix_use = 0, pds_use = 0;
+        bool ok = true;
+        // D[tmem] = A B^T with both operands K-major over d (S or S^T, and dP or dP^T)
+        auto issue_kk = [&](uint32_t col, uint32_t a_addr, uint32_t b_addr) {
+            const uint64_t ad = ptx::sdesc_sw128(a_addr, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_elect(tmem + col, ad + off, bd + off, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+        };
+        // D[tmem] (+)= A[tmem, bf16] B with B a [128 rows x d] tile read MN-major
+        auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, bool accumulate) {
+            const uint64_t bd = ptx::sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + kk * 8, bd + ((kk * 2048) >> 4), IDESC_ACC,
+                                  (accumulate || kk > 0) ? 1u : 0u);
+        };
+        for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
+            const BwdUnit w = bwd_unit<MODE>(u, p);
+            if (w.steps == 0) continue;
+            ok = wait_warp(bar(C::B_FIXFULL), fix_use & 1u, abort_flag, limit);
+            ++fix_use;
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t f0 = sb + C::SMEM_FIX, f1 = sb + C::SMEM_FIX + C::TILE_BYTES;
+            for (int s = 0; s < w.steps; ++s) {
+                const uint32_t slot = it % C::STAGES, ph = (it / C::STAGES) & 1u;
+                ++it;
+                ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t s0 = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES, s1 = s0 + C::TILE_BYTES;
+                // MODE 0: S^T = K Q^T, dP^T = V dO^T.  MODE 1: S = Q K^T, dP = dO V^T.
+                issue_kk(C::COL_S, f0, s0);
+                issue_kk(C::COL_DP, f1, s1);
+                ptx::mma_commit_elect(bar(C::B_SDP));
+                ok = wait_warp(bar(C::B_PDS), pds_use & 1u, abort_flag, limit);
+                ++pds_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
+                if constexpr (MODE == 0) {
+                    issue_acc(C::COL_A0, C::COL_S, s1, s > 0);   // dV += P^T dO
+                    issue_acc(C::COL_A1, C::COL_DP, s0, s > 0);  // dK += dS^T Q
+                } else {
+                    issue_acc(C::COL_A0, C::COL_S, s0, s > 0);   // dQ += dS K
+                }
+                ptx::mma_commit_elect(bar(C::B_EMPTY + slot));
+            }
+            if (!ok) break;
+            ptx::mma_commit_elect(bar(C::B_FIXEMPTY));
+            ptx::mma_commit_elect(bar(C::B_ACC));
+        }
+        ptx::mma_commit_elect(bar(C::B_DRAIN));
+        drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================================================================ compute
+        const int row = warp * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + C::COL_S, t_dp = tmem + lane_off + C::COL_DP;
+        const uint32_t t_a0 = tmem + lane_off + C::COL_A0, t_a1 = tmem + lane_off + C::COL_A1;
+        uint32_t it = 0, sdp_use = 0, acc_use = 0;
+        bool ok = true;
+        for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
+            const BwdUnit w = bwd_unit<MODE>(u, p);
+            const int r_abs = w.tile * BM + row;  // this thread's key (MODE 0) or query (MODE 1)
+            // MODE 1: the row's lse (log2 units) and D
+            float row_lse2 = 0.f, row_d = 0.f;
+            if constexpr (MODE == 1) {
+                if (r_abs < p.N) {
+                    const size_t idx = static_cast<size_t>(w.zfix) * p.N + r_abs;
+                    row_lse2 = __ldg(p.lse + idx) * 1.4426950408889634f;
+                    row_d = __ldg(p.dsum + idx);
+                }
+            }
+            int ilo, ihi;  // this row's visible column interval (absolute positions)
+            if constexpr (MODE == 0)
+                key_query_interval(p, r_abs, w.L, ilo, ihi);
+            else
+                query_key_interval(p, r_abs, w.L, ilo, ihi);
+            for (int s = 0; ok && s < w.steps; ++s) {
+                const int n_t = w.hi - w.lo;
+                const int g = MODE == 0 ? s / n_t : 0;
+                const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
+                const uint32_t slot = it % C::STAGES, ph = (it / C::STAGES) & 1u;
+                ++it;
+                const float *vec = reinterpret_cast<const float *>(smem + C::SMEM_VEC) + slot * 2 * BM;
+                if constexpr (MODE == 0) {
+                    // the per-column lse and D were staged with the tiles of this slot
+                    ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
+                    if (!ok) break;
+                }
+                ok = wait_warp(bar(C::B_SDP), sdp_use & 1u, abort_flag, limit);
+                ++sdp_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
+                (void)g;
+                // columns of this tile the row sees: [c_lo, c_hi] relative to the tile
+                const int c0 = t * BN;
+                const int c_hi = min(ihi, c0 + BN - 1) - c0;
+                const int c_lo = max(ilo, c0) - c0;
+                const bool none = c_hi < c_lo;
+                const bool covers = !none && c_lo == 0 && c_hi == BN - 1;
+                const bool need_mask = !__all_sync(0xffffffffu, covers);
+                const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
+                const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t sr[32], dr[32];
+                    ptx::tmem_ld32(t_s + 32 * c, sr);
+                    ptx::tmem_ld32(t_dp + 32 * c, dr);
+                    ptx::tmem_wait_ld();
+                    uint32_t pk[16], dk16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float pp[2], ds[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = 32 * c + 2 * e + h;
+                            const float lse2 = MODE == 0 ? vec[col] : row_lse2;
+                            const float dv = MODE == 0 ? vec[BM + col] : row_d;
+                            float pv = ptx::ex2(fmaf(__uint_as_float(sr[2 * e + h]), p.sl2, -lse2));
+                            if (need_mask && static_cast<uint32_t>(col) - base > span) pv = 0.f;
+                            pp[h] = pv;
+                            ds[h] = pv * (__uint_as_float(dr[2 * e + h]) - dv);
+                        }
+                        pk[e] = ptx::pack_bf16x2(pp[0], pp[1]);
+                        dk16[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+                    }
+                    if constexpr (MODE == 0) {
+                        ptx::tmem_st16(t_s + 16 * c, pk);     // P^T, A of dV += P^T dO
+                        ptx::tmem_st16(t_dp + 16 * c, dk16);  // dS^T, A of dK += dS^T Q
+                    } else {
+                        ptx::tmem_st16(t_s + 16 * c, dk16);   // dS, A of dQ += dS K
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS));
+            }
+            if (!ok) break;
+            // epilogue: MODE 0 writes dV and scale * dK of the key rows, MODE 1 scale * dQ;
+            // a unit with nothing to stream writes zeros
+            const bool has = w.steps > 0;
+            if (has) {
+                ok = wait_warp(bar(C::B_ACC), acc_use & 1u, abort_flag, limit);
+                ++acc_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
+            }
+#pragma unroll 1
+            for (int a = 0; a < (MODE == 0 ? 2 : 1); ++a) {
+                __nv_bfloat16 *out = MODE == 0 ? (a == 0 ? p.dv : p.dk) : p.dq;
+                const float mul = (MODE == 0 && a == 0) ? 1.f : p.scale;
+                const uint32_t t_acc = a == 0 ? t_a0 : t_a1;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    if (has) {
+                        ptx::tmem_ld32(t_acc + 32 * c, r);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = 0u;
+                    }
+                    if (r_abs < p.N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(w.zfix) * p.N + r_abs) * D +
+                                                               32 * c);
+#pragma unroll
+                        for (int g4 = 0; g4 < 4; ++g4) {
+                            uint4 val;
+                            val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 0]) * mul,
+                                                     __uint_as_float(r[8 * g4 + 1]) * mul);
+                            val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * mul,
+                                                     __uint_as_float(r[8 * g4 + 3]) * mul);
+                            val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * mul,
+                                                     __uint_as_float(r[8 * g4 + 5]) * mul);
+                            val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * mul,
+                                                     __uint_as_float(r[8 * g4 + 7]) * mul);
+                            dst[g4] = val;
+                        }
+                    }
+                }
+            }
+            // the accumulators are read: release them for the next unit's first product
+            ptx::tc_fence_before();
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == BWD_WARP_MMA) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}

@@ -1122,6 +1122,8 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
     wait_warp(ptx::smem_addr(&bar), 0u, &abort_flag, limit_ns);
 }
 
+#include "attn_bwd.cuh"
+
 }  // namespace attn
 
 // ====================================================================== host side
@@ -1138,6 +1140,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool ready;
+    bool bwd_ready;
     int sms;
 };
 
@@ -1503,6 +1506,90 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
     return ATTN_OK;
 }
 
+
+// ------------------------------------------------------------------ backward
+// one-time shared-memory opt-in of the backward kernels on the current device
+int bwd_setup(int *sms_out) {
+    int rc = device_setup(sms_out);
+    if (rc != ATTN_OK) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (!di.bwd_ready) {
+        if ((e = cudaFuncSetAttribute(attn::attn_bwd_kernel<64, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      attn::BwdCfg<64>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_bwd_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      attn::BwdCfg<64>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_bwd_kernel<128, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      attn::BwdCfg<128>::SMEM_ALLOC)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn::attn_bwd_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      attn::BwdCfg<128>::SMEM_ALLOC)) != cudaSuccess)
+            return cuda_fail(e);
+        di.bwd_ready = true;
+    }
+    return ATTN_OK;
+}
+
+template <int D>
+int launch_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B,
+               int Hq, int Hkv, int N, int causal, int window, float scale, cudaStream_t stream, int sms) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported);
+    const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
+    CUtensorMap mq, mk, mv, mdo;
+    int rc;
+    if ((rc = encode_map(enc, &mq, q, D, N, BHq)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mk, k, D, N, BHkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mv, v, D, N, BHkv)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mdo, dout, D, N, BHq)) != ATTN_OK) return rc;
+    // D = rowsum(dO o O), one warp per row
+    const long long rows = BHq * N;
+    attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), dsum, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    attn::BwdParams p;
+    p.dsum = dsum;
+    p.lse = lse;
+    p.dq = static_cast<__nv_bfloat16 *>(dq);
+    p.dk = static_cast<__nv_bfloat16 *>(dk);
+    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.key_len = key_len;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.N = N;
+    p.group = Hq / Hkv;
+    p.causal = causal;
+    p.window = window >= N ? 0 : window;  // a window of N or more keys excludes nothing
+    p.sym = (p.window > 0 && !causal) ? 1 : 0;
+    p.n_kv = (N + attn::BN - 1) / attn::BN;
+    p.sl2 = scale * 1.4426950408889634f;
+    p.scale = scale;
+    p.timeout_ns = attn::WAIT_LIMIT_NS;
+    p.div_bhkv = attn::make_fastdiv(static_cast<uint32_t>(BHkv));
+    p.div_hkv = attn::make_fastdiv(static_cast<uint32_t>(Hkv));
+    p.div_bhq = attn::make_fastdiv(static_cast<uint32_t>(BHq));
+    p.div_hq = attn::make_fastdiv(static_cast<uint32_t>(Hq));
+    p.div_group = attn::make_fastdiv(static_cast<uint32_t>(p.group));
+    // dK, dV: one unit per (key tile, batch, kv head)
+    p.num_units = static_cast<int>(BHkv * p.n_kv);
+    int grid = p.num_units < sms ? p.num_units : sms;
+    attn::attn_bwd_kernel<D, 0><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv,
+                                                                                                  mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    // dQ: one unit per (query tile, batch, query head)
+    p.num_units = static_cast<int>(BHq * p.n_kv);
+    grid = p.num_units < sms ? p.num_units : sms;
+    attn::attn_bwd_kernel<D, 1><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv,
+                                                                                                  mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1641,6 +1728,27 @@ int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, floa
         (e = cudaMemcpyAsync(hlse, dlse, lse_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         return cuda_fail(e);
     return ATTN_OK;
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+             void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B, int Hq, int Hkv, int N, int d,
+             int causal, int window, float scale, void *stream) {
+    if (!dout || !dq || !dk || !dv || !dsum) return ATTN_ERR_NULLPTR;
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc != ATTN_OK) return rc;
+    const long long units = static_cast<long long>(B) * Hq * ((N + attn::BN - 1) / attn::BN);
+    if (units > INT_MAX) return ATTN_ERR_SHAPE;
+    if (misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
+        misaligned(dsum, 4) || (key_len && misaligned(key_len, 4)))
+        return ATTN_ERR_ALIGN;
+    int sms = 0;
+    if ((rc = bwd_setup(&sms)) != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 64)
+        return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, dsum, key_len, B, Hq, Hkv, N, causal, window,
+                              scale, s, sms);
+    return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, dsum, key_len, B, Hq, Hkv, N, causal, window, scale,
+                           s, sms);
 }
 
 const char *attn_status_str(int status) {

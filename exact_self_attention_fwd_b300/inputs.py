@@ -111,3 +111,10 @@ def make_qkv_decode(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, seed: i
     v = torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32)
     return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
             v.to(torch.bfloat16).contiguous())
+
+
+def make_dout(B: int, Hq: int, N: int, d: int, seed: int):
+    """Upstream gradient dO [B,Hq,N,d] for the backward pass: CPU bf16, N(0,1) from a
+    generator seeded with `seed`, rounded to bf16."""
+    g = torch.Generator().manual_seed(int(seed))
+    return torch.randn((B, Hq, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16).contiguous()

@@ -176,6 +176,37 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_
                  int Hkv, int N, int d, int causal, int window, float scale, void *stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd's output with respect to Q, K and V. The FlashAttention-3
+ * review (deepmi.me, "Results: Backward Pass" and "Computation and memory requirements")
+ * names the backward pass and puts its cost at about 2.5 times the forward's; it gives no
+ * formulas, so the gradients are those of the forward's definition by the chain rule:
+ *
+ *   P  = exp(scale S - lse)   the forward's softmax weights (0 where masked or padded)
+ *   dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D)
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO
+ *
+ * dK and dV of a key/value head sum over the Hq / Hkv query heads that read it.
+ *
+ *   q, k, v, B, Hq, Hkv, N, d, causal, window, scale, stream   as for attn_fwd (the same
+ *            values the forward ran with)
+ *   key_len  NULL, or the device int32 [B] valid lengths of attn_fwd_padded
+ *   o, lse   device, the forward's outputs for these inputs (read): o bf16 [B, Hq, N, d],
+ *            16-byte aligned; lse fp32 [B, Hq, N] (natural log, -inf on padded rows)
+ *   dout     device, bf16 [B, Hq, N, d], 16-byte aligned (read): the gradient of o
+ *   dq       device, bf16 [B, Hq, N, d], 16-byte aligned (written)
+ *   dk, dv   device, bf16 [B, Hkv, N, d], 16-byte aligned (written); rows of keys that no
+ *            query sees (padding) are written as zeros
+ *   dsum     device, fp32 [B, Hq, N], 4-byte aligned, caller-owned (written): D above
+ *
+ * Arithmetic: S and dP accumulate in fp32 on the tensor cores; P and dS are rounded to
+ * bf16 as the operands of the dV, dK and dQ products, which accumulate in fp32; the
+ * results are rounded to bf16 once. Errors as for attn_fwd; asynchronous on `stream`.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B,
+             int Hq, int Hkv, int N, int d, int causal, int window, float scale, void *stream);
+
+/*
  * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that cannot allocate device
  * memory. The pages have no counterpart to this entry point; it exists for users of the
  * library.
