@@ -72,6 +72,12 @@ def flops(w: Workload) -> int:
     return 4 * w.B * w.Hq * visible_pairs(w.N, w.causal, w.window) * w.d
 
 
+def bwd_flops(w: Workload) -> int:
+    """FLOPs of one backward pass over the visible pairs: five products of d MACs per
+    pair (S and dP recomputed, then dV, dK and dQ), 2.5 times the forward's."""
+    return 10 * w.B * w.Hq * visible_pairs(w.N, w.causal, w.window) * w.d
+
+
 def hbm_bytes(w: Workload) -> int:
     """Algorithmic bytes: Q, K, V read once (bf16), O written (bf16), LSE written (fp32)."""
     q = w.B * w.Hq * w.N * w.d * 2
@@ -432,6 +438,42 @@ def measure_decode(ea, w: DecodeWorkload, dev, steps: int, warmup: int, seed_off
     return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
 
 
+def measure_bwd(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
+    """Device time per attn_bwd call (its three kernels) on workload w, with O and LSE
+    from attn_fwd computed once beforehand; per-call CUDA events, L2 flushed between
+    calls."""
+    import torch
+    from exact_self_attention_fwd_b300.inputs import make_dout
+    q, k, v = make_qkv(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed + seed_offset, w.q_head0_scale)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    dod = make_dout(w.B, w.Hq, w.N, w.d, w.seed + 100 + seed_offset).to(dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        out, lse = ea.attn_fwd(qd, kd, vd, causal=w.causal, window=w.window, scale=w.scale, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(ea.bwd_workspace_size(w.B, w.Hq, w.N, w.d), dtype=torch.uint8, device=dev)
+
+    def call():
+        ea.attn_bwd(qd, kd, vd, out, lse, dod, causal=w.causal, window=w.window, scale=w.scale,
+                    dq=dq, dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_l2(flush)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
+
+
 def measure_fp8(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
     """Device time per call of (a) attn_fwd_fp8 on pre-quantised operands and (b) the
     block quantisation of Q, K and V (three attn_quantize_e4m3 calls), per-call CUDA
@@ -640,6 +682,16 @@ def run_ours(args, w: Workload):
             "quantize_us": t_quant * 1e6, "quantize_gbs": qbytes / t_quant / 1e9,
             "timing": "per-call CUDA events, L2 flushed between calls",
             "entry": "attn_fwd_fp8 (e4m3 Q, K, V with 128-row block scales); attn_quantize_e4m3 timed apart"}
+        for name in ("gpt2_small", "gqa_8k"):
+            bw = WORKLOADS[name]
+            t_bwd = measure_bwd(ea, bw, dev, args.summary_steps, 3, seed_offset=rank)
+            tf = bwd_flops(bw) / t_bwd / 1e12
+            summary[name + "_bwd"] = {
+                "tflops": tf, "us_per_call": t_bwd * 1e6, "bound": "tensor",
+                "frac": tf / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                "flops_note": "5 products of d MACs per visible pair (2.5 x the forward)",
+                "timing": "per-call CUDA events, L2 flushed between calls",
+                "entry": "attn_bwd (row-term preprocess + fused dK/dV/dQ kernel + dQ conversion)"}
         for name, dw in DECODE_WORKLOADS.items():
             t_call = measure_decode(ea, dw, dev, args.summary_steps, 5, seed_offset=rank)
             gbs = decode_hbm_bytes(dw) / t_call / 1e9

@@ -61,7 +61,10 @@ def _declare(lib):
     lib.attn_fwd_fp8.restype = i
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_host.restype = i
-    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, ctypes.c_size_t,
+                             vp]
     lib.attn_bwd.restype = i
     lib.attn_status_str.argtypes = [i]
     lib.attn_status_str.restype = ctypes.c_char_p
@@ -166,45 +169,57 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
     return out, lse
 
 
+def bwd_workspace_size(B: int, Hq: int, N: int, d: int) -> int:
+    """Bytes of workspace attn_bwd needs (D = rowsum(dO o O) per query row, fp32)."""
+    return int(load().attn_bwd_workspace_size(B, Hq, N, d))
+
+
+def bwd_row_sums(workspace, B: int, Hq: int, N: int):
+    """View of D = rowsum(dO o O) that attn_bwd wrote into `workspace`: fp32 [B, Hq, N]."""
+    import torch
+    return workspace[: B * Hq * N * 4].view(torch.float32).view(B, Hq, N)
+
+
 def attn_bwd(q, k, v, out, lse, dout, causal: bool = False, window: int = 0, scale: float | None = None,
-             key_len=None, dq=None, dk=None, dv=None, dsum=None, stream=None):
+             key_len=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Gradients (dq [B,Hq,N,d], dk, dv [B,Hkv,N,d], all bf16) of attn_fwd's output for the
     upstream gradient dout [B,Hq,N,d] bf16; out and lse are the forward's results for the
-    same q, k, v, mask and scale. dsum (fp32 [B,Hq,N], allocated when None) receives
-    D = rowsum(dout * out). Asynchronous on `stream`.
+    same q, k, v, mask and scale. workspace: a uint8 CUDA tensor of at least
+    bwd_workspace_size(B, Hq, N, d) bytes (allocated when None). Asynchronous on `stream`.
     """
     import torch
     B, Hq, Hkv, N, d = _check_tensors(q, k, v)
     dev = q.device
+    if dev.type != "cuda" or k.device != dev or v.device != dev:
+        raise ValueError("q, k, v must be CUDA tensors on one device")
     for name, t in (("out", out), ("dout", dout)):
         if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != dev:
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like q")
     if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != dev:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, Hq, N]")
-    if dev.type != "cuda" or k.device != dev or v.device != dev:
-        raise ValueError("q, k, v must be CUDA tensors on one device")
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    if dsum is None:
-        dsum = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         if t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != dev:
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor shaped like its input")
-    if tuple(dsum.shape) != (B, Hq, N) or dsum.dtype != torch.float32 or not dsum.is_contiguous() \
-            or dsum.device != dev:
-        raise ValueError("dsum must be a contiguous fp32 CUDA tensor [B, Hq, N]")
+    need = bwd_workspace_size(B, Hq, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor on q's device")
     if key_len is not None and (key_len.device != dev or key_len.dtype != torch.int32 or key_len.numel() != B
                                 or not key_len.is_contiguous()):
         raise ValueError("key_len must be a contiguous int32 CUDA tensor with B entries")
     L = load()
     with torch.cuda.device(dev):
         rc = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dsum.data_ptr(),
+                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                         None if key_len is None else key_len.data_ptr(), B, Hq, Hkv, N, d,
-                        int(bool(causal)), int(window), float(scale), _stream_handle(stream, dev))
+                        int(bool(causal)), int(window), float(scale), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _check(rc)
     return dq, dk, dv
 

@@ -17,9 +17,15 @@
 //                          warps, then dV += P^T dO and dK += dS^T Q accumulate in tensor
 //                          memory across the whole stream
 //   bwd kernel, MODE 1     query-stationary: holds Q_i, dO_i and streams (K_j, V_j):
-//                          S = Q K^T, dP = dO V^T, dS, then dQ += dS K (no atomics)
+//                          S = Q K^T, dP = dO V^T, dS, then dQ += dS K (no atomics, so
+//                          the result does not depend on the order of the key tiles)
+// Each streamed 128-row tile is taken in two sub-steps of 64 rows (queries in MODE 0,
+// keys in MODE 1), with two tensor-memory buffers for S and dP: the tensor core computes
+// one sub-step's S and dP while the compute warps turn the other's into P and dS.
 // Warps: 0-3 compute (one tensor-memory row each thread), 4 TMA producer, 5 MMA issuer,
-// 6-7 idle. Tensor memory: S (or S^T) [0,128), dP [128,256), two accumulators from 256.
+// 6-7 idle. Tensor memory: sub-step buffer h at [128h, 128h + 128) with S (or S^T) in
+// its first 64 columns and dP in the other 64 (P and dS, bf16, over their first 32),
+// then the accumulators from column 256.
 #pragma once
 
 constexpr int BWD_THREADS = 256;
@@ -50,14 +56,15 @@ struct BwdCfg {
     static constexpr int SMEM_VEC = SMEM_RING + STAGES * 2 * TILE_BYTES;  // per slot: lse2, D
     static constexpr int SMEM_BAR = SMEM_VEC + STAGES * 2 * BM * 4;
     static constexpr int B_FIXFULL = 0, B_FIXEMPTY = 1, B_FULL = 2, B_EMPTY = 2 + STAGES;
-    static constexpr int B_SDP = 2 + 2 * STAGES;  // S and dP computed
-    static constexpr int B_PDS = B_SDP + 1;       // P (MODE 0) and dS written (4 warps)
-    static constexpr int B_ACC = B_PDS + 1;       // accumulators of the unit complete
+    static constexpr int B_SDP = 2 + 2 * STAGES;  // 2: S and dP of sub-step h computed
+    static constexpr int B_PDS = B_SDP + 2;       // 2: P (MODE 0) and dS of sub-step h written (4 warps)
+    static constexpr int B_ACC = B_PDS + 2;       // accumulators of the unit complete
     static constexpr int B_DRAIN = B_ACC + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_ALLOC = SMEM_CTL + 16 + 1024;
-    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_A0 = 256, COL_A1 = 256 + D;
+    static constexpr uint32_t COL_BUF = 128;  // sub-step buffer h starts at column 128h
+    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_A0 = 256, COL_A1 = 256 + D;
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
@@ -210,8 +217,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_init(bar(C::B_FULL + s), 1);
             ptx::mbar_init(bar(C::B_EMPTY + s), 1);
         }
-        ptx::mbar_init(bar(C::B_SDP), 1);
-        ptx::mbar_init(bar(C::B_PDS), 4);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(bar(C::B_SDP + h), 1);
+            ptx::mbar_init(bar(C::B_PDS + h), 4);
+        }
         ptx::mbar_init(bar(C::B_ACC), 1);
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                                        bar(C::B_FIXFULL), c * 64, w.tile * BM, w.zfix);
             }
             for (int s = 0; ok && s < w.steps; ++s) {
-                // MODE 0: step s = (head g of the group, query tile i); MODE 1: key tile
+                // MODE 0: step s = (head g of the group, query tile t); MODE 1: key tile t
                 const int n_t = w.hi - w.lo;
                 const int g = MODE == 0 ? s / n_t : 0;
                 const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
@@ -301,27 +310,57 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
     } else if (warp == BWD_WARP_MMA) {
         // ================================================================ MMA issuer
-        constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
+        // All 32 lanes run this loop with identical values; each MMA and commit is
+        // issued by one elected lane. MMAs of one thread run in issue order, so a product
+        // may overwrite tensor-memory columns that earlier products read.
+        constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, 64, false);
         constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(BM, D, true);
-        uint32_t it = 0, fix_use = 0, pds_use = 0;
+        uint32_t it = 0, fix_use = 0, pds_use0 = 0, pds_use1 = 0;
         bool ok = true;
-        // D[tmem] = A B^T with both operands K-major over d (S or S^T, and dP or dP^T)
-        auto issue_kk = [&](uint32_t col, uint32_t a_addr, uint32_t b_addr) {
-            const uint64_t ad = ptx::sdesc_sw128(a_addr, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(b_addr, 16, 1024);
+        // sub-step h: S (S^T) and dP (dP^T) = A B^T over d, both operands K-major; B is
+        // rows 64h .. 64h + 63 of the streamed tile (8 KB into each 128-row slab)
+        auto issue_sdp = [&](int h, uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
+            const uint32_t col = C::COL_BUF * h;
+            const uint64_t a0d = ptx::sdesc_sw128(a0, 16, 1024), a1d = ptx::sdesc_sw128(a1, 16, 1024);
+            const uint64_t b0d = ptx::sdesc_sw128(b0 + h * 8192, 16, 1024);
+            const uint64_t b1d = ptx::sdesc_sw128(b1 + h * 8192, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_elect(tmem + col, ad + off, bd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                ptx::mma_ss_elect(tmem + col + C::COL_S, a0d + off, b0d + off, IDESC_S, kk > 0 ? 1u : 0u);
             }
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_elect(tmem + col + C::COL_DP, a1d + off, b1d + off, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit_elect(bar(C::B_SDP + h));
         };
-        // D[tmem] (+)= A[tmem, bf16] B with B a [128 rows x d] tile read MN-major
-        auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, bool accumulate) {
+        // D[tmem] (+)= A[tmem, bf16] B for sub-step h: A = 64 packed rows' worth of P / dS
+        // (32 columns), B = rows 64h .. 64h + 63 of a [128 x d] tile read MN-major
+        auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, int h, bool accumulate) {
             const uint64_t bd = ptx::sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + kk * 8, bd + ((kk * 2048) >> 4), IDESC_ACC,
-                                  (accumulate || kk > 0) ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int kr = 4 * h + k4;  // 16-row step within the tile
+                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + k4 * 8, bd + ((kr * 2048) >> 4), IDESC_ACC,
+                                  (accumulate || k4 > 0) ? 1u : 0u);
+            }
+        };
+        // the accumulating products of sub-step h, once the compute warps wrote P / dS
+        auto issue_products = [&](int h, uint32_t s0, uint32_t s1, bool accumulate) -> bool {
+            uint32_t &use = h ? pds_use1 : pds_use0;
+            if (!wait_warp(bar(C::B_PDS + h), use & 1u, abort_flag, limit)) return false;
+            ++use;
+            ptx::tc_fence_after();
+            const uint32_t buf = C::COL_BUF * h;
+            if constexpr (MODE == 0) {
+                issue_acc(C::COL_A0, buf + C::COL_S, s1, h, accumulate);   // dV += P^T dO
+                issue_acc(C::COL_A1, buf + C::COL_DP, s0, h, accumulate);  // dK += dS^T Q
+            } else {
+                issue_acc(C::COL_A0, buf + C::COL_S, s0, h, accumulate);   // dQ += dS K
+            }
+            return true;
         };
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
@@ -331,6 +370,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t f0 = sb + C::SMEM_FIX, f1 = sb + C::SMEM_FIX + C::TILE_BYTES;
+            uint32_t prev_s0 = 0, prev_s1 = 0, prev_slot = 0;
             for (int s = 0; s < w.steps; ++s) {
                 const uint32_t slot = it % C::STAGES, ph = (it / C::STAGES) & 1u;
                 ++it;
@@ -338,23 +378,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t s0 = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES, s1 = s0 + C::TILE_BYTES;
-                // MODE 0: S^T = K Q^T, dP^T = V dO^T.  MODE 1: S = Q K^T, dP = dO V^T.
-                issue_kk(C::COL_S, f0, s0);
-                issue_kk(C::COL_DP, f1, s1);
-                ptx::mma_commit_elect(bar(C::B_SDP));
-                ok = wait_warp(bar(C::B_PDS), pds_use & 1u, abort_flag, limit);
-                ++pds_use;
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if constexpr (MODE == 0) {
-                    issue_acc(C::COL_A0, C::COL_S, s1, s > 0);   // dV += P^T dO
-                    issue_acc(C::COL_A1, C::COL_DP, s0, s > 0);  // dK += dS^T Q
-                } else {
-                    issue_acc(C::COL_A0, C::COL_S, s0, s > 0);   // dQ += dS K
+                // order: S, dP of (s, 0); products of (s - 1, 1); S, dP of (s, 1); products
+                // of (s, 0). Buffer h is rewritten only after the products that read its P
+                // and dS were issued, and the tensor core always has the next sub-step's
+                // S and dP to compute while the compute warps work.
+                issue_sdp(0, f0, f1, s0, s1);
+                if (s > 0) {
+                    if (!(ok = issue_products(1, prev_s0, prev_s1, true))) break;
+                    ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
                 }
-                ptx::mma_commit_elect(bar(C::B_EMPTY + slot));
+                issue_sdp(1, f0, f1, s0, s1);
+                if (!(ok = issue_products(0, s0, s1, s > 0))) break;
+                prev_s0 = s0;
+                prev_s1 = s1;
+                prev_slot = slot;
             }
             if (!ok) break;
+            if (!(ok = issue_products(1, prev_s0, prev_s1, true))) break;
+            ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
             ptx::mma_commit_elect(bar(C::B_FIXEMPTY));
             ptx::mma_commit_elect(bar(C::B_ACC));
         }
@@ -365,9 +406,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // ================================================================ compute
         const int row = warp * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_off + C::COL_S, t_dp = tmem + lane_off + C::COL_DP;
-        const uint32_t t_a0 = tmem + lane_off + C::COL_A0, t_a1 = tmem + lane_off + C::COL_A1;
-        uint32_t it = 0, sdp_use = 0, acc_use = 0;
+        uint32_t it = 0, sdp_use0 = 0, sdp_use1 = 0, acc_use = 0;
         bool ok = true;
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
@@ -398,54 +437,72 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
                     if (!ok) break;
                 }
-                ok = wait_warp(bar(C::B_SDP), sdp_use & 1u, abort_flag, limit);
-                ++sdp_use;
-                if (!ok) break;
-                ptx::tc_fence_after();
                 (void)g;
                 // columns of this tile the row sees: [c_lo, c_hi] relative to the tile
                 const int c0 = t * BN;
                 const int c_hi = min(ihi, c0 + BN - 1) - c0;
                 const int c_lo = max(ilo, c0) - c0;
                 const bool none = c_hi < c_lo;
-                const bool covers = !none && c_lo == 0 && c_hi == BN - 1;
-                const bool need_mask = !__all_sync(0xffffffffu, covers);
                 const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
                 const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t sr[32], dr[32];
-                    ptx::tmem_ld32(t_s + 32 * c, sr);
-                    ptx::tmem_ld32(t_dp + 32 * c, dr);
-                    ptx::tmem_wait_ld();
-                    uint32_t pk[16], dk16[16];
+                for (int h = 0; h < 2; ++h) {
+                    // sub-step h: columns 64h .. 64h + 63 of the tile
+                    const bool covers = !none && c_lo <= 64 * h && c_hi >= 64 * h + 63;
+                    const bool need_mask = !__all_sync(0xffffffffu, covers);
+                    uint32_t &use = h ? sdp_use1 : sdp_use0;
+                    ok = wait_warp(bar(C::B_SDP + h), use & 1u, abort_flag, limit);
+                    ++use;
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t t_s = tmem + lane_off + C::COL_BUF * h + C::COL_S;
+                    const uint32_t t_dp = tmem + lane_off + C::COL_BUF * h + C::COL_DP;
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t sr[32], dr[32];
+                        ptx::tmem_ld32(t_s + 32 * c, sr);
+                        ptx::tmem_ld32(t_dp + 32 * c, dr);
+                        const int cb = 64 * h + 32 * c;  // first column of the chunk in the tile
+                        ptx::tmem_wait_ld();
+                        uint32_t pk[16], dk16[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float pp[2], ds[2];
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            float4 l4, d4;
+                            if constexpr (MODE == 0) {
+                                l4 = *reinterpret_cast<const float4 *>(vec + cb + 4 * e4);
+                                d4 = *reinterpret_cast<const float4 *>(vec + BM + cb + 4 * e4);
+                            } else {
+                                l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
+                                d4 = make_float4(row_d, row_d, row_d, row_d);
+                            }
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                            float pp[4], ds[4];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int col = 32 * c + 2 * e + h;
-                            const float lse2 = MODE == 0 ? vec[col] : row_lse2;
-                            const float dv = MODE == 0 ? vec[BM + col] : row_d;
-                            float pv = ptx::ex2(fmaf(__uint_as_float(sr[2 * e + h]), p.sl2, -lse2));
-                            if (need_mask && static_cast<uint32_t>(col) - base > span) pv = 0.f;
-                            pp[h] = pv;
-                            ds[h] = pv * (__uint_as_float(dr[2 * e + h]) - dv);
+                            for (int q = 0; q < 4; ++q) {
+                                const int e = 4 * e4 + q;
+                                float pv = ptx::ex2(fmaf(__uint_as_float(sr[e]), p.sl2, -lv[q]));
+                                if (need_mask && static_cast<uint32_t>(cb + e) - base > span) pv = 0.f;
+                                pp[q] = pv;
+                                ds[q] = pv * (__uint_as_float(dr[e]) - dv[q]);
+                            }
+                            pk[2 * e4] = ptx::pack_bf16x2(pp[0], pp[1]);
+                            pk[2 * e4 + 1] = ptx::pack_bf16x2(pp[2], pp[3]);
+                            dk16[2 * e4] = ptx::pack_bf16x2(ds[0], ds[1]);
+                            dk16[2 * e4 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
                         }
-                        pk[e] = ptx::pack_bf16x2(pp[0], pp[1]);
-                        dk16[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+                        if constexpr (MODE == 0) {
+                            ptx::tmem_st16(t_s + 16 * c, pk);     // P^T, A of dV += P^T dO
+                            ptx::tmem_st16(t_dp + 16 * c, dk16);  // dS^T, A of dK += dS^T Q
+                        } else {
+                            ptx::tmem_st16(t_s + 16 * c, dk16);   // dS, A of dQ += dS K
+                        }
                     }
-                    if constexpr (MODE == 0) {
-                        ptx::tmem_st16(t_s + 16 * c, pk);     // P^T, A of dV += P^T dO
-                        ptx::tmem_st16(t_dp + 16 * c, dk16);  // dS^T, A of dK += dS^T Q
-                    } else {
-                        ptx::tmem_st16(t_s + 16 * c, dk16);   // dS, A of dQ += dS K
-                    }
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS + h));
                 }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS));
             }
             if (!ok) break;
             // epilogue: MODE 0 writes dV and scale * dK of the key rows, MODE 1 scale * dQ;
@@ -461,7 +518,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             for (int a = 0; a < (MODE == 0 ? 2 : 1); ++a) {
                 __nv_bfloat16 *out = MODE == 0 ? (a == 0 ? p.dv : p.dk) : p.dq;
                 const float mul = (MODE == 0 && a == 0) ? 1.f : p.scale;
-                const uint32_t t_acc = a == 0 ? t_a0 : t_a1;
+                const uint32_t t_acc = tmem + lane_off + (a == 0 ? C::COL_A0 : C::COL_A1);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -491,7 +548,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     }
                 }
             }
-            // the accumulators are read: release them for the next unit's first product
+            // the accumulators are read: the next unit's first products overwrite them
             ptx::tc_fence_before();
         }
     }

@@ -1532,10 +1532,16 @@ int bwd_setup(int *sms_out) {
     return ATTN_OK;
 }
 
+// workspace of the backward: D = rowsum(dO o O) of every query row, fp32
+size_t bwd_workspace(int B, int Hq, int N) {
+    const size_t b = static_cast<size_t>(B) * Hq * N * sizeof(float);
+    return (b + 255) / 256 * 256;
+}
+
 template <int D>
 int launch_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-               const void *dout, void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B,
-               int Hq, int Hkv, int N, int causal, int window, float scale, cudaStream_t stream, int sms) {
+               const void *dout, void *dq, void *dk, void *dv, const int *key_len, int B, int Hq, int Hkv,
+               int N, int causal, int window, float scale, void *workspace, cudaStream_t stream, int sms) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
     const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
@@ -1545,6 +1551,7 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     if ((rc = encode_map(enc, &mk, k, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mdo, dout, D, N, BHq)) != ATTN_OK) return rc;
+    float *dsum = static_cast<float *>(workspace);
     // D = rowsum(dO o O), one warp per row
     const long long rows = BHq * N;
     attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
@@ -1730,25 +1737,31 @@ int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, floa
     return ATTN_OK;
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int N, int d) {
+    if (B < 1 || Hq < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    return bwd_workspace(B, Hq, N);
+}
+
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
-             void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B, int Hq, int Hkv, int N, int d,
-             int causal, int window, float scale, void *stream) {
-    if (!dout || !dq || !dk || !dv || !dsum) return ATTN_ERR_NULLPTR;
+             void *dq, void *dk, void *dv, const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
+             int window, float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULLPTR;
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
     if (rc != ATTN_OK) return rc;
     const long long units = static_cast<long long>(B) * Hq * ((N + attn::BN - 1) / attn::BN);
     if (units > INT_MAX) return ATTN_ERR_SHAPE;
     if (misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
-        misaligned(dsum, 4) || (key_len && misaligned(key_len, 4)))
+        misaligned(workspace, 256) || (key_len && misaligned(key_len, 4)))
         return ATTN_ERR_ALIGN;
+    if (workspace_bytes < bwd_workspace(B, Hq, N)) return ATTN_ERR_WORKSPACE;
     int sms = 0;
     if ((rc = bwd_setup(&sms)) != ATTN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d == 64)
-        return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, dsum, key_len, B, Hq, Hkv, N, causal, window,
-                              scale, s, sms);
-    return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, dsum, key_len, B, Hq, Hkv, N, causal, window, scale,
-                           s, sms);
+        return launch_bwd<64>(q, k, v, o, lse, dout, dq, dk, dv, key_len, B, Hq, Hkv, N, causal, window, scale,
+                              workspace, s, sms);
+    return launch_bwd<128>(q, k, v, o, lse, dout, dq, dk, dv, key_len, B, Hq, Hkv, N, causal, window, scale,
+                           workspace, s, sms);
 }
 
 const char *attn_status_str(int status) {

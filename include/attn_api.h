@@ -179,7 +179,8 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_
  * attn_bwd -- gradients of attn_fwd's output with respect to Q, K and V. The FlashAttention-3
  * review (deepmi.me, "Results: Backward Pass" and "Computation and memory requirements")
  * names the backward pass and puts its cost at about 2.5 times the forward's; it gives no
- * formulas, so the gradients are those of the forward's definition by the chain rule:
+ * formulas, so the gradients are those of the forward's definition by the chain rule,
+ * with the forward's O and LSE taken as inputs:
  *
  *   P  = exp(scale S - lse)   the forward's softmax weights (0 where masked or padded)
  *   dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D)
@@ -196,15 +197,20 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_
  *   dq       device, bf16 [B, Hq, N, d], 16-byte aligned (written)
  *   dk, dv   device, bf16 [B, Hkv, N, d], 16-byte aligned (written); rows of keys that no
  *            query sees (padding) are written as zeros
- *   dsum     device, fp32 [B, Hq, N], 4-byte aligned, caller-owned (written): D above
+ *   workspace  device, 256-byte aligned, at least attn_bwd_workspace_size(B, Hq, N, d)
+ *            bytes, caller-owned (overwritten): D of every query row, fp32 [B, Hq, N]
  *
  * Arithmetic: S and dP accumulate in fp32 on the tensor cores; P and dS are rounded to
- * bf16 as the operands of the dV, dK and dQ products, which accumulate in fp32; the
- * results are rounded to bf16 once. Errors as for attn_fwd; asynchronous on `stream`.
+ * bf16 as the operands of the dV, dK and dQ products, which accumulate in fp32 in a
+ * fixed order (the result does not vary from run to run); the results are rounded to
+ * bf16 once. Errors as for attn_fwd, and ATTN_ERR_WORKSPACE for a short workspace;
+ * asynchronous on `stream`.
  */
+size_t attn_bwd_workspace_size(int B, int Hq, int N, int d);
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-             const void *dout, void *dq, void *dk, void *dv, float *dsum, const int *key_len, int B,
-             int Hq, int Hkv, int N, int d, int causal, int window, float scale, void *stream);
+             const void *dout, void *dq, void *dk, void *dv, const int *key_len, int B, int Hq,
+             int Hkv, int N, int d, int causal, int window, float scale, void *workspace,
+             size_t workspace_bytes, void *stream);
 
 /*
  * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that cannot allocate device

@@ -46,6 +46,7 @@ def test_workload_accounting():
     for name, w in WORKLOADS.items():
         assert bench.visible_pairs(w.N, w.causal, w.window) == expect[name]
         assert bench.flops(w) == 4 * w.B * w.Hq * expect[name] * w.d
+        assert bench.bwd_flops(w) * 2 == bench.flops(w) * 5
     w = WORKLOADS["gqa_8k"]
     assert bench.hbm_bytes(w) == (2 * 32 * 8192 * 128 * 2) * 2 + 2 * (2 * 8 * 8192 * 128 * 2) + 2 * 32 * 8192 * 4
 

@@ -104,9 +104,9 @@ def check_bwd(B, Hq, Hkv, N, d, causal, window, seed, key_len=None, q_head0_scal
         out = torch.from_numpy(o_ref).to(torch.bfloat16).to(DEV)
         lse = torch.from_numpy(lse_ref).float().to(DEV)
         o_given = out.double().cpu()
-    dsum = torch.full((B, Hq, N), float("nan"), device=DEV)
+    ws = torch.full((ea.bwd_workspace_size(B, Hq, N, d),), 0xFF, dtype=torch.uint8, device=DEV)  # NaN fill
     dq, dk, dv = ea.attn_bwd(qd, kd, vd, out, lse, dod, causal=causal, window=window, scale=scale,
-                             key_len=kl, dsum=dsum)
+                             key_len=kl, workspace=ws)
     torch.cuda.synchronize()
     assert ea.device_error() == ea.ATTN_OK
     rq, rk, rv = oracle.attn_ref_bwd(q, k, v, do, causal=causal, window=window, scale=scale,
@@ -116,7 +116,8 @@ def check_bwd(B, Hq, Hkv, N, d, causal, window, seed, key_len=None, q_head0_scal
         # D = rowsum(dO o O) from the given bf16 values: exact products, an fp32 sum of d
         # of them (error <= d 2^-24 of the sum of magnitudes)
         prod = do.double().numpy() * o_given.numpy()
-        assert np.all(np.abs(_np(dsum) - prod.sum(-1)) <= d * 2.0 ** -24 * np.abs(prod).sum(-1) + 1e-30), \
+        dsum = _np(ea.bwd_row_sums(ws, B, Hq, N))
+        assert np.all(np.abs(dsum - prod.sum(-1)) <= d * 2.0 ** -24 * np.abs(prod).sum(-1) + 1e-30), \
             f"{label}: D differs from rowsum(dO o O)"
     rms = max(rms_rows(rq), rms_rows(rk), rms_rows(rv))
     if pipeline:
@@ -192,10 +193,18 @@ def test_bwd_rejects_bad_arguments():
     with pytest.raises(ValueError):
         ea.attn_bwd(q, k, v, out, lse, out[:, :1].contiguous())
     L = ea.load()
-    rc = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), out.data_ptr(),
-                    None, k.data_ptr(), v.data_ptr(), lse.data_ptr(), None, 1, 2, 1, 64, 64, 0, 0, 0.125, None)
-    assert rc == ea.ATTN_ERR_NULLPTR
-    rc = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), out.data_ptr(),
-                    q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), None, 1, 2, 1, 64, 96, 0, 0, 0.125,
-                    None)
-    assert rc == ea.ATTN_ERR_UNSUPPORTED
+    need = ea.bwd_workspace_size(1, 2, 64, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), out.data_ptr(),
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), None, 1, 2, 1, 64, 64, 0, 0, 0.125, ws.data_ptr(), need, None]
+    bad = list(args)
+    bad[6] = None
+    assert L.attn_bwd(*bad) == ea.ATTN_ERR_NULLPTR
+    bad = list(args)
+    bad[14] = 96
+    assert L.attn_bwd(*bad) == ea.ATTN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[19] = need - 1
+    assert L.attn_bwd(*bad) == ea.ATTN_ERR_WORKSPACE
+    assert L.attn_bwd(*args) == ea.ATTN_OK
+    torch.cuda.synchronize()
