@@ -170,14 +170,19 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
 
 
 def bwd_workspace_size(B: int, Hq: int, N: int, d: int) -> int:
-    """Bytes of workspace attn_bwd needs (D = rowsum(dO o O) per query row, fp32)."""
+    """Bytes of workspace attn_bwd needs (lse log2(e) and D = rowsum(dO o O) per query
+    row, fp32, rows padded to a multiple of 128)."""
     return int(load().attn_bwd_workspace_size(B, Hq, N, d))
 
 
 def bwd_row_sums(workspace, B: int, Hq: int, N: int):
-    """View of D = rowsum(dO o O) that attn_bwd wrote into `workspace`: fp32 [B, Hq, N]."""
+    """View of D = rowsum(dO o O) that attn_bwd wrote into `workspace`: fp32 [B, Hq, N]
+    (the workspace holds lse log2(e) and then D, each head's rows padded to a multiple
+    of 128)."""
     import torch
-    return workspace[: B * Hq * N * 4].view(torch.float32).view(B, Hq, N)
+    n_pad = (N + 127) // 128 * 128
+    f = workspace[: 2 * B * Hq * n_pad * 4].view(torch.float32)
+    return f[B * Hq * n_pad:].view(B, Hq, n_pad)[:, :, :N]
 
 
 def attn_bwd(q, k, v, out, lse, dout, causal: bool = False, window: int = 0, scale: float | None = None,

@@ -9,7 +9,8 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO   (dK, dV summed over a group's heads)
 //
 // Three kernels:
-//   bwd_preprocess_kernel  D = rowsum(dO o O) in fp32 (one warp per row)
+//   bwd_preprocess_kernel  per query row lse log2(e) and D = rowsum(dO o O) in fp32 (one
+//                          warp per row), each head's rows padded to a multiple of 128
 //   bwd kernel, MODE 0     key-stationary: a CTA holds K_j, V_j of one key tile and
 //                          streams (Q_i, dO_i) over every query head of the group and
 //                          every query tile that sees the keys: S^T = K Q^T and
@@ -33,11 +34,11 @@ constexpr int BWD_WARP_TMA = 4;
 constexpr int BWD_WARP_MMA = 5;
 
 struct BwdParams {
-    const float *dsum;              // D = dO . O per query row, fp32 [B * Hq * N]
-    const float *lse;               // forward LSE, natural log, [B * Hq * N]
+    const float *lse2;  // lse log2(e) per query row, fp32 [B * Hq * N_pad] (0 past N)
+    const float *dsum;  // D = dO . O per query row, fp32 [B * Hq * N_pad] (0 past N)
     __nv_bfloat16 *dq, *dk, *dv;
     const int *key_len;
-    int B, Hq, Hkv, N, group;
+    int B, Hq, Hkv, N, N_pad, group;
     int causal, window, sym;
     int n_kv, num_units;
     float sl2, scale;
@@ -69,15 +70,28 @@ struct BwdCfg {
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
 
-// D_i = sum_c dO[i, c] O[i, c] in fp32, one warp per row
+// Per query row of each head (N_pad rows, one warp each): lse log2(e) and
+// D = sum_c dO O in fp32; rows from N to N_pad get zeros.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o,
                                                              const __nv_bfloat16 *__restrict__ dout,
-                                                             float *__restrict__ dsum, long long rows) {
+                                                             const float *__restrict__ lse,
+                                                             float *__restrict__ lse2, float *__restrict__ dsum,
+                                                             long long BH, int N, int N_pad) {
     constexpr int PER = D / 32;  // bf16 per lane
-    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    if (prow >= BH * N_pad) return;
+    const long long h = prow / N_pad;
+    const int i = static_cast<int>(prow - h * N_pad);
+    if (i >= N) {
+        if (lane == 0) {
+            lse2[prow] = 0.f;
+            dsum[prow] = 0.f;
+        }
+        return;
+    }
+    const long long row = h * N + i;
     const __nv_bfloat16 *a = o + row * D + lane * PER;
     const __nv_bfloat16 *b = dout + row * D + lane * PER;
     float acc = 0.f;
@@ -94,7 +108,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) dsum[row] = acc;
+    if (lane == 0) {
+        lse2[prow] = __ldg(lse + row) * 1.4426950408889634f;
+        dsum[prow] = acc;
+    }
 }
 
 __device__ __forceinline__ int bwd_valid_len(const BwdParams &p, int b) {
@@ -277,21 +294,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ok = wait_warp(bar(C::B_EMPTY + slot), ph, abort_flag, limit);
                 if (!ok) break;
                 ++it;
-                if constexpr (MODE == 0) {
-                    // the streamed query tile's lse (in log2 units) and D, one value per
-                    // column, staged beside the tiles for the compute warps
-                    float *vec = reinterpret_cast<float *>(smem + C::SMEM_VEC) + slot * 2 * BM;
-#pragma unroll
-                    for (int r = 0; r < BM / 32; ++r) {
-                        const int qq = t * BM + r * 32 + lane;
-                        const size_t idx = static_cast<size_t>(zs) * p.N + qq;
-                        vec[r * 32 + lane] = qq < p.N ? __ldg(p.lse + idx) * 1.4426950408889634f : 0.f;
-                        vec[BM + r * 32 + lane] = qq < p.N ? __ldg(p.dsum + idx) : 0.f;
-                    }
-                    __syncwarp();
-                }
-                ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES);
                 const uint32_t dst = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES;
+                if constexpr (MODE == 0) {
+                    // the streamed query tile's lse log2(e) and D (one value per column)
+                    // land beside the tiles on the same barrier
+                    const uint32_t vec = sb + C::SMEM_VEC + slot * 2 * BM * 4;
+                    const size_t idx = static_cast<size_t>(zs) * p.N_pad + t * BM;
+                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES + 2 * BM * 4);
+                    ptx::bulk_load_elect(vec, p.lse2 + idx, BM * 4, bar(C::B_FULL + slot));
+                    ptx::bulk_load_elect(vec + BM * 4, p.dsum + idx, BM * 4, bar(C::B_FULL + slot));
+                } else {
+                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES);
+                }
 #pragma unroll
                 for (int c = 0; c < C::NCHUNK; ++c) {
                     ptx::tma_load_3d_elect(dst + c * C::CHUNK_BYTES, str0, bar(C::B_FULL + slot), c * 64, t * BM, zs);
@@ -415,8 +429,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             float row_lse2 = 0.f, row_d = 0.f;
             if constexpr (MODE == 1) {
                 if (r_abs < p.N) {
-                    const size_t idx = static_cast<size_t>(w.zfix) * p.N + r_abs;
-                    row_lse2 = __ldg(p.lse + idx) * 1.4426950408889634f;
+                    const size_t idx = static_cast<size_t>(w.zfix) * p.N_pad + r_abs;
+                    row_lse2 = __ldg(p.lse2 + idx);
                     row_d = __ldg(p.dsum + idx);
                 }
             }

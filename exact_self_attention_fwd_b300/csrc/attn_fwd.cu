@@ -1532,10 +1532,11 @@ int bwd_setup(int *sms_out) {
     return ATTN_OK;
 }
 
-// workspace of the backward: D = rowsum(dO o O) of every query row, fp32
+// workspace of the backward: lse log2(e), then D = rowsum(dO o O), of every query row
+// (fp32), each head's rows padded to a multiple of the tile
+long long bwd_n_pad(int N) { return (static_cast<long long>(N) + attn::BM - 1) / attn::BM * attn::BM; }
 size_t bwd_workspace(int B, int Hq, int N) {
-    const size_t b = static_cast<size_t>(B) * Hq * N * sizeof(float);
-    return (b + 255) / 256 * 256;
+    return 2 * static_cast<size_t>(B) * Hq * bwd_n_pad(N) * sizeof(float);
 }
 
 template <int D>
@@ -1551,16 +1552,19 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     if ((rc = encode_map(enc, &mk, k, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mdo, dout, D, N, BHq)) != ATTN_OK) return rc;
-    float *dsum = static_cast<float *>(workspace);
-    // D = rowsum(dO o O), one warp per row
-    const long long rows = BHq * N;
-    attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), dsum, rows);
+    const int n_pad = static_cast<int>(bwd_n_pad(N));
+    float *lse2 = static_cast<float *>(workspace);
+    float *dsum = lse2 + BHq * n_pad;
+    // lse log2(e) and D = rowsum(dO o O), one warp per (padded) row
+    const long long prows = BHq * n_pad;
+    attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((prows + 7) / 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse, lse2, dsum, BHq, N,
+        n_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     attn::BwdParams p;
+    p.lse2 = lse2;
     p.dsum = dsum;
-    p.lse = lse;
     p.dq = static_cast<__nv_bfloat16 *>(dq);
     p.dk = static_cast<__nv_bfloat16 *>(dk);
     p.dv = static_cast<__nv_bfloat16 *>(dv);
@@ -1569,6 +1573,7 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.N = N;
+    p.N_pad = n_pad;
     p.group = Hq / Hkv;
     p.causal = causal;
     p.window = window >= N ? 0 : window;  // a window of N or more keys excludes nothing
@@ -1749,7 +1754,7 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
     if (rc != ATTN_OK) return rc;
     const long long units = static_cast<long long>(B) * Hq * ((N + attn::BN - 1) / attn::BN);
-    if (units > INT_MAX) return ATTN_ERR_SHAPE;
+    if (units > INT_MAX || static_cast<long long>(B) * Hq * bwd_n_pad(N) > INT_MAX) return ATTN_ERR_SHAPE;
     if (misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
         misaligned(workspace, 256) || (key_len && misaligned(key_len, 4)))
         return ATTN_ERR_ALIGN;

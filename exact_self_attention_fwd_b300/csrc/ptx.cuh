@@ -119,6 +119,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
         ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// global to shared memory, completing on `bar`; issued by one elected lane
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                   int x, int y, int z) {
     asm volatile(

@@ -198,7 +198,8 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_
  *   dk, dv   device, bf16 [B, Hkv, N, d], 16-byte aligned (written); rows of keys that no
  *            query sees (padding) are written as zeros
  *   workspace  device, 256-byte aligned, at least attn_bwd_workspace_size(B, Hq, N, d)
- *            bytes, caller-owned (overwritten): D of every query row, fp32 [B, Hq, N]
+ *            bytes, caller-owned (overwritten): lse log2(e), then D, of every query row,
+ *            fp32 [B, Hq, ceil(N / 128) x 128] each (rows past N zero)
  *
  * Arithmetic: S and dP accumulate in fp32 on the tensor cores; P and dS are rounded to
  * bf16 as the operands of the dV, dK and dQ products, which accumulate in fp32 in a
