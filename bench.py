@@ -736,6 +736,43 @@ def run_ours(args, w: Workload):
     return 0
 
 
+def run_bwd(args, w: Workload):
+    """The backward pass as the timed step (one GPU): attn_bwd on the workload with O and
+    LSE from one attn_fwd call made beforehand, per-call CUDA events, L2 flushed between
+    calls. Used to measure and profile the backward kernels on their own."""
+    import torch
+
+    import exact_self_attention_fwd_b300 as ea
+    world, _, local = dist_env()
+    if world != 1:
+        raise RuntimeError("--pass bwd runs on one GPU")
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: this benchmark times the CUDA library only")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    ea.load()
+    t = measure_bwd(ea, w, dev, args.steps, args.warmup)
+    if ea.device_error() != ea.ATTN_OK:
+        raise RuntimeError("kernel wait timed out")
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tf = bwd_flops(w) / t / 1e12
+    line = {
+        "metric": "attention bwd TFLOP/s (10 d FLOP per visible pair, 2.5 x the forward)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rounded to bf16)",
+        "config": {"workload": w.name, "pass": "bwd", "shape": w.note,
+                   "l2": "256 MiB buffer written then read before every call; per-call CUDA events exclude it"},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": f"bwd_preprocess_kernel<{w.d}> + attn_bwd_kernel<{w.d}, 0> + attn_bwd_kernel<{w.d}, 1>"},
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -743,6 +780,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time attn_bwd on the workload instead (one GPU, no reference arm)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline field (0 = skip)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
@@ -760,6 +799,11 @@ def main(argv=None):
             return 0
         return run_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
+    if args.which == "bwd":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the forward"}))
+            return 0
+        return run_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
