@@ -691,7 +691,7 @@ def run_ours(args, w: Workload):
                 "frac": tf / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
                 "flops_note": "5 products of d MACs per visible pair (2.5 x the forward)",
                 "timing": "per-call CUDA events, L2 flushed between calls",
-                "entry": "attn_bwd (row-term preprocess + fused dK/dV/dQ kernel + dQ conversion)"}
+                "entry": "attn_bwd (row-term preprocess + dK/dV kernel + dQ kernel)"}
         for name, dw in DECODE_WORKLOADS.items():
             t_call = measure_decode(ea, dw, dev, args.summary_steps, 5, seed_offset=rank)
             gbs = decode_hbm_bytes(dw) / t_call / 1e9
