@@ -82,6 +82,9 @@ def _declare(lib):
     lib.attn_ref_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                      ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p]
     lib.attn_ref_bwd_f64.restype = ctypes.c_int
+    lib.attn_ref_quantize_e4m3_blocks_f64.argtypes = [f64p, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_uint8),
+                                                      f64p]
+    lib.attn_ref_quantize_e4m3_blocks_f64.restype = ctypes.c_int
     lib.attn_ref_bwd_given_o_f64.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, i64, ctypes.c_int,
                                              i64, ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p,
                                              f64p]
@@ -274,18 +277,64 @@ def attn_ref_f64in(q, k, v, causal: bool = False, window: int = 0, scale: float 
     return o, lse
 
 
+def hadamard(d: int) -> np.ndarray:
+    """The Sylvester Hadamard matrix of order d (a power of two), entries +-1, fp64:
+    H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]], so H H^T = d I."""
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def incoherent(x, signs) -> np.ndarray:
+    """Incoherent processing of the FlashAttention-3 review: x' = x M with the random
+    orthogonal M = diag(signs) H / sqrt(d) (signs +-1, H the Sylvester Hadamard
+    matrix). x bf16 (or real) [..., d]; returns fp64 [..., d]. Since M M^T = I,
+    Q' K'^T = Q K^T: attention on (Q', K', V) is attention on (Q, K, V)."""
+    xv = x.double().numpy() if hasattr(x, "double") else np.asarray(x, dtype=np.float64)
+    s = np.asarray(signs, dtype=np.float64)
+    d = xv.shape[-1]
+    return (xv * s) @ hadamard(d) / np.sqrt(d)
+
+
+def quantize_e4m3_blocks_f64(x, rows: int = 128):
+    """Block quantisation of real values x [..., N, d] (fp64, exact arithmetic): codes
+    uint8 [..., N, d] and fp64 scales [heads, ceil(N / rows)] with scale = amax / 448."""
+    xv = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    *lead, N, d = xv.shape
+    BH = int(np.prod(lead)) if lead else 1
+    codes = np.empty(xv.shape, dtype=np.uint8)
+    nblk = (N + rows - 1) // rows
+    scales = np.empty((BH, nblk), dtype=np.float64)
+    rc = load().attn_ref_quantize_e4m3_blocks_f64(
+        xv.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), BH, N, d, rows,
+        codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+        scales.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError("bad arguments")
+    return codes, scales
+
+
 def attn_ref_fp8(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
-                 rows=None, block_rows: int = 128, per_tensor: bool = False):
+                 rows=None, block_rows: int = 128, per_tensor: bool = False, signs=None):
     """FP8 attention as the FlashAttention-3 review describes it: Q, K and V are block
     quantised to e4m3 (blocks of block_rows x d per head, or one scale for the whole
     tensor when per_tensor), then attention is computed exactly (fp64) on the
-    dequantised values. Returns (o, lse) like attn_ref, plus the dequantised inputs."""
+    dequantised values. With `signs` (+-1 per channel), Q and K first go through
+    incoherent processing (x M, M = diag(signs) H / sqrt(d)) and their rotated values
+    are block quantised in exact arithmetic. Returns (o, lse) like attn_ref, plus the
+    dequantised inputs."""
     d = q.shape[-1]
     if scale is None:
         scale = 1.0 / float(np.sqrt(d))
     deq = []
-    for t in (q, k, v):
-        if per_tensor:
+    for i, t in enumerate((q, k, v)):
+        if signs is not None and i < 2:
+            codes, sc = quantize_e4m3_blocks_f64(incoherent(t, signs), rows=block_rows)
+            deq.append(dequantize_e4m3_blocks(codes, sc, rows=block_rows))
+        elif per_tensor:
             flat = t.reshape(1, 1, -1, d)
             codes, sc = quantize_e4m3_blocks(flat, rows=flat.shape[2])
             deq.append(dequantize_e4m3_blocks(codes, sc, rows=flat.shape[2]).reshape(tuple(t.shape)))

@@ -357,6 +357,36 @@ int attn_ref_quantize_e4m3_blocks(const uint16_t *x, int64_t BH, int64_t N, int6
 }
 
 /*
+ * Block quantisation of real-valued inputs [BH, N, d] (fp64), for the incoherent-processing
+ * path, whose rotated values are not bf16: for block k of head h, amax = max |x|,
+ * code = e4m3(x * 448 / amax) and scale = amax / 448, all in fp64 (the exact definition);
+ * an all-zero block gets scale 1 and zero codes. Writes codes [BH, N, d] and scales
+ * [BH, ceil(N / rows)].
+ */
+int attn_ref_quantize_e4m3_blocks_f64(const double *x, int64_t BH, int64_t N, int64_t d, int64_t rows,
+                                      uint8_t *codes, double *scales) {
+    if (!x || !codes || !scales || BH < 1 || N < 1 || d < 1 || rows < 1) return -1;
+    const int64_t nblk = (N + rows - 1) / rows;
+    for (int64_t h = 0; h < BH; ++h) {
+        for (int64_t k = 0; k < nblk; ++k) {
+            const int64_t r0 = k * rows, r1 = (r0 + rows < N) ? r0 + rows : N;
+            double amax = 0.0;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c) {
+                    const double a = fabs(x[(h * N + r) * d + c]);
+                    if (a > amax) amax = a;
+                }
+            scales[h * nblk + k] = amax > 0.0 ? amax / 448.0 : 1.0;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = 0; c < d; ++c)
+                    codes[(h * N + r) * d + c] =
+                        amax > 0.0 ? e4m3_round(x[(h * N + r) * d + c] * (448.0 / amax)) : (uint8_t)0;
+        }
+    }
+    return 0;
+}
+
+/*
  * Backward pass: gradients of the attention forward (o above) with respect to q, k, v
  * for an upstream gradient do_ = dL/do, restated from the chain rule through the
  * definition (the pages only say that the backward pass exists and costs about 2.5x the

@@ -15,6 +15,7 @@
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -112,3 +113,87 @@ def test_block_scaling_beats_tensor_scaling_with_outliers():
     # asserted, with a margin (on this data the ratio is about 1.3)
     r_blk, r_ten = worst_rel_rmse(o_blk), worst_rel_rmse(o_ten)
     assert r_blk * 1.2 < r_ten, (r_blk, r_ten)
+
+
+# ------------------------------------------------------------ incoherent processing
+def test_hadamard_is_sylvester_and_orthogonal():
+    import scipy.linalg
+    for d in (1, 2, 4, 8, 16, 32, 64, 128):
+        h = oracle.hadamard(d)
+        assert np.array_equal(h, scipy.linalg.hadamard(d).astype(np.float64))
+        assert np.array_equal(h @ h.T, d * np.eye(d))
+    with pytest.raises(ValueError):
+        oracle.hadamard(96)
+
+
+def test_incoherent_one_hot_rows():
+    # e_i M = s_i H[i, :] / sqrt(d): row i of the Hadamard matrix, with channel i's sign
+    d = 128
+    rng = np.random.default_rng(43)
+    s = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    h = oracle.hadamard(d)
+    for i in (0, 1, 5, 64, 127):
+        x = np.zeros((1, d))
+        x[0, i] = 1.0
+        y = oracle.incoherent(x, s)
+        assert np.allclose(y[0], s[i] * h[i] / np.sqrt(d), atol=1e-15, rtol=0)
+    # Sylvester entries (-1)^popcount(i & j)
+    for i, j in ((3, 5), (127, 127), (64, 63), (96, 33)):
+        assert h[i, j] == (-1) ** bin(i & j).count("1")
+
+
+def test_incoherent_preserves_scores_and_attention():
+    # Q' K'^T = Q M M^T K^T = Q K^T, so attention on (Q', K', V) equals attention on (Q, K, V)
+    g = torch.Generator().manual_seed(44)
+    B, H, N, d = 1, 2, 130, 128
+    q, k, v = (torch.randn(B, H, N, d, generator=g).bfloat16() for _ in range(3))
+    s = np.where(np.random.default_rng(45).random(d) < 0.5, -1.0, 1.0)
+    qi, ki = oracle.incoherent(q, s), oracle.incoherent(k, s)
+    assert np.allclose(qi[0, 0] @ ki[0, 0].T, q[0, 0].double().numpy() @ k[0, 0].double().numpy().T,
+                       atol=1e-11, rtol=0)
+    o1, l1 = oracle.attn_ref_f64in(qi, ki, v.double().numpy(), True, 0, 0.088)
+    o0, l0 = oracle.attn_ref(q, k, v, causal=True, scale=0.088)
+    assert np.allclose(o1, o0, atol=1e-12, rtol=0) and np.allclose(l1, l0, atol=1e-12, rtol=0)
+
+
+def test_real_valued_quantiser_bounds_and_exact_case():
+    g = torch.Generator().manual_seed(46)
+    x = (torch.randn(2, 300, 128, generator=g) * 3).double().numpy()
+    codes, scales = oracle.quantize_e4m3_blocks_f64(x, rows=128)
+    deq = oracle.dequantize_e4m3_blocks(codes, scales, rows=128)
+    for h in range(2):
+        for kb in range(3):
+            blk = x[h, 128 * kb:128 * (kb + 1)]
+            sc = float(scales[h, kb])
+            assert sc == np.abs(blk).max() / 448.0
+            err = np.abs(deq[h, 128 * kb:128 * (kb + 1)] - blk)
+            assert np.all(err <= np.maximum(np.abs(blk) * 2.0 ** -4, sc * 2.0 ** -10) * (1 + 1e-12))
+    # with a block maximum of 448 both quantisers scale by exactly 1, so on bf16 inputs
+    # the exact-arithmetic one and the fp32 one give the same codes
+    xb = (torch.randn(1, 128, 64, generator=g) * 40).bfloat16()
+    xb[0, 0, 0] = 448.0
+    xb = xb.clamp(-448, 448)
+    c32, s32 = oracle.quantize_e4m3_blocks(xb, rows=128)
+    c64, s64 = oracle.quantize_e4m3_blocks_f64(xb.double().numpy(), rows=128)
+    assert np.array_equal(c32, c64) and float(s32[0, 0]) == float(s64[0, 0]) == 1.0
+
+
+def test_incoherent_processing_helps_with_outlier_channels():
+    # a few channels of Q and K far larger than the rest: with block scales the small
+    # channels lose their precision to the outliers' scale; the rotation spreads each
+    # outlier over all channels first. The error of FP8 attention against exact
+    # attention drops (the direction the review states; the margin is this data's).
+    g = torch.Generator().manual_seed(47)
+    B, H, N, d = 1, 2, 256, 128
+    boost = torch.ones(d)
+    boost[[7, 70]] = 60.0
+    q = (torch.randn(B, H, N, d, generator=g) * boost).bfloat16()
+    k = (torch.randn(B, H, N, d, generator=g) * boost * 0.02).bfloat16()
+    v = torch.randn(B, H, N, d, generator=g).bfloat16()
+    s = np.where(np.random.default_rng(48).random(d) < 0.5, -1.0, 1.0)
+    o_ex, _ = oracle.attn_ref(q, k, v, causal=True, scale=0.088)
+    o_blk, _, _ = oracle.attn_ref_fp8(q, k, v, causal=True, scale=0.088)
+    o_inc, _, _ = oracle.attn_ref_fp8(q, k, v, causal=True, scale=0.088, signs=s)
+    e_blk = float(np.sqrt(np.mean((o_blk - o_ex) ** 2)))
+    e_inc = float(np.sqrt(np.mean((o_inc - o_ex) ** 2)))
+    assert e_inc * 1.5 < e_blk, (e_inc, e_blk)
