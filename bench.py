@@ -475,9 +475,10 @@ def measure_bwd(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int 
 
 
 def measure_fp8(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
-    """Device time per call of (a) attn_fwd_fp8 on pre-quantised operands and (b) the
-    block quantisation of Q, K and V (three attn_quantize_e4m3 calls), per-call CUDA
-    events with L2 flushed between calls."""
+    """Device time per call of (a) attn_fwd_fp8 on pre-quantised operands, (b) the block
+    quantisation of Q, K and V (three attn_quantize_e4m3 calls) and (c) the same with
+    incoherent processing of Q and K (attn_quantize_e4m3_hadamard), per-call CUDA events
+    with L2 flushed between calls."""
     import torch
     q, k, v = make_qkv(w.B, w.Hq, w.Hkv, w.N, w.d, w.seed + seed_offset, w.q_head0_scale)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -496,8 +497,17 @@ def measure_fp8(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int 
         for t in (qd, kd, vd):
             ea.quantize_e4m3(t, stream=stream)
 
+    from exact_self_attention_fwd_b300.inputs import make_signs
+    signs = make_signs(w.d, w.seed + 1) if w.d == 128 else None
+
+    def quant_hadamard():
+        # incoherent processing of Q and K, plain block quantisation of V
+        ea.quantize_e4m3_hadamard(qd, signs, stream=stream)
+        ea.quantize_e4m3_hadamard(kd, signs, stream=stream)
+        ea.quantize_e4m3(vd, stream=stream)
+
     res = []
-    for fn in (attn, quant):
+    for fn in (attn, quant, quant_hadamard):
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
@@ -512,7 +522,7 @@ def measure_fp8(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int 
                 ends[i].record(stream)
         torch.cuda.synchronize(dev)
         res.append(sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps)
-    return res[0], res[1]
+    return res[0], res[1], res[2]
 
 
 def run_decode(args, w: DecodeWorkload):
@@ -672,7 +682,7 @@ def run_ours(args, w: Workload):
                              "gbs": hbm_bytes(ww) / t_call / 1e9, "bound": r["bound"],
                              "frac": r["frac"], "timing": how}
         fw = WORKLOADS["gqa_8k"]
-        t_attn, t_quant = measure_fp8(ea, fw, dev, args.summary_steps, 5, seed_offset=rank)
+        t_attn, t_quant, t_quant_h = measure_fp8(ea, fw, dev, args.summary_steps, 5, seed_offset=rank)
         fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         qbytes = (fw.B * fw.Hq + 2 * fw.B * fw.Hkv) * fw.N * fw.d * 3  # read bf16, write e4m3
         summary["gqa_8k_fp8"] = {
@@ -680,8 +690,10 @@ def run_ours(args, w: Workload):
             "frac": flops(fw) / t_attn / 1e12 / fp8_peak,
             "peak_note": "fp8 peak = 2 x measured bf16 burst peak (nominal dense ratio)",
             "quantize_us": t_quant * 1e6, "quantize_gbs": qbytes / t_quant / 1e9,
+            "quantize_hadamard_us": t_quant_h * 1e6, "quantize_hadamard_gbs": qbytes / t_quant_h / 1e9,
             "timing": "per-call CUDA events, L2 flushed between calls",
-            "entry": "attn_fwd_fp8 (e4m3 Q, K, V with 128-row block scales); attn_quantize_e4m3 timed apart"}
+            "entry": ("attn_fwd_fp8 (e4m3 Q, K, V with 128-row block scales); attn_quantize_e4m3 and "
+                      "attn_quantize_e4m3_hadamard (incoherent processing of Q and K) timed apart")}
         for name in ("gpt2_small", "gqa_8k"):
             bw = WORKLOADS[name]
             t_bwd = measure_bwd(ea, bw, dev, args.summary_steps, 3, seed_offset=rank)

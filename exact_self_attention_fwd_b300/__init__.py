@@ -7,7 +7,8 @@ from ._lib import (ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_NULLPTR, ATTN_ERR_SCR
                    ATTN_OK, AttnError,
                    attn_bwd, attn_fwd, attn_fwd_decode, attn_fwd_fp8, attn_fwd_host, bwd_row_sums,
                    bwd_workspace_size, decode_workspace_size,
-                   device_error, header_functions, load, quantize_e4m3, selftest_wait_timeout,
+                   device_error, header_functions, load, quantize_e4m3, quantize_e4m3_hadamard, selftest_wait_timeout,
+                   sign_masks,
                    status_str, version)
 
 __all__ = [
@@ -15,6 +16,6 @@ __all__ = [
     "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_SCRATCH_LIMIT",
     "AttnError", "attn_bwd", "attn_fwd", "bwd_row_sums", "bwd_workspace_size",
     "attn_fwd_decode", "attn_fwd_fp8", "attn_fwd_host", "decode_workspace_size", "device_error",
-    "header_functions", "quantize_e4m3",
+    "header_functions", "quantize_e4m3", "quantize_e4m3_hadamard", "sign_masks",
     "load", "selftest_wait_timeout", "status_str", "version",
 ]

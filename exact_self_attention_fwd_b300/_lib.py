@@ -56,6 +56,8 @@ def _declare(lib):
     lib.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
     lib.attn_fwd_decode_noalloc.restype = i
     lib.attn_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, vp]
+    lib.attn_quantize_e4m3_hadamard.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp, vp, i, i, i, vp]
+    lib.attn_quantize_e4m3_hadamard.restype = i
     lib.attn_quantize_e4m3.restype = i
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_fp8.restype = i
@@ -286,6 +288,35 @@ def quantize_e4m3(x, stream=None):
     with torch.cuda.device(x.device):
         rc = load().attn_quantize_e4m3(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), BH, N, d,
                                        _stream_handle(stream, x.device))
+    _check(rc)
+    return codes, scales
+
+
+def sign_masks(signs) -> tuple[int, int]:
+    """The two 64-bit masks of attn_quantize_e4m3_hadamard for 128 signs (+1 or -1):
+    bit c set where signs[c] is -1."""
+    sg = [float(x) for x in signs]
+    if len(sg) != 128 or any(x not in (1.0, -1.0) for x in sg):
+        raise ValueError("signs must be 128 values, each +1 or -1")
+    bits = sum(1 << c for c, x in enumerate(sg) if x < 0)
+    return bits & ((1 << 64) - 1), bits >> 64
+
+
+def quantize_e4m3_hadamard(x, signs, stream=None):
+    """Incoherent processing (x M, M = diag(signs) H / sqrt(128)) then block quantisation
+    of a CUDA bf16 tensor [..., N, 128]: e4m3 codes (uint8, same shape) and fp32 scales
+    [heads, ceil(N / 128)] (attn_quantize_e4m3_hadamard). Use the same signs for Q and K."""
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.device.type != "cuda" or x.dim() < 2:
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [..., N, d]")
+    N, d = x.shape[-2], x.shape[-1]
+    BH = x.numel() // (N * d)
+    lo, hi = sign_masks(signs)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((BH, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = load().attn_quantize_e4m3_hadamard(x.data_ptr(), lo, hi, codes.data_ptr(), scales.data_ptr(), BH, N,
+                                                d, _stream_handle(stream, x.device))
     _check(rc)
     return codes, scales
 

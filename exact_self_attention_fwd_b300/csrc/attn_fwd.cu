@@ -1052,6 +1052,107 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16 
     }
 }
 
+// Incoherent processing, then block quantisation (the FlashAttention-3 review's FP8 path):
+// the rows are rotated by the random orthogonal M = diag(s) H / sqrt(128), s = +-1 per
+// channel and H the Sylvester Hadamard matrix of order 128, and the rotated block is
+// quantised as above. One CTA per (block of 128 rows, head); a warp takes 4 rows at a
+// time, 8 lanes per row, lane l holding elements 16 (l mod 8) .. 16 (l mod 8) + 15 of
+// row l / 8. y = (x o s) H is formed in fp32 by the seven butterfly stages of the fast
+// Walsh-Hadamard transform (element-index bits 0-3 inside a lane, bits 4-6 across the
+// row's 8 lanes by shuffles). Codes are e4m3(y * (448 / amax)) and the block's scale is
+// (amax / 448) / sqrt(128), so that code x scale approximates x M; an all-zero block
+// gets scale 1.
+__global__ void __launch_bounds__(256, 2) quantize_hadamard_e4m3_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                                     uint8_t *__restrict__ codes,
+                                                                     float *__restrict__ scales, int N, int nblk,
+                                                                     unsigned long long neg_lo,
+                                                                     unsigned long long neg_hi) {
+    constexpr int D = 128, PASSES = BM / 8 / 4;  // 8 warps x 4 rows per pass
+    const int blk = blockIdx.x, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int part = lane & 7;  // which 16 channels of the row
+    // channels 16 part .. 16 part + 15 whose sign is flipped (bit c of the 128-bit mask)
+    const uint32_t neg = static_cast<uint32_t>((part < 4 ? neg_lo : neg_hi) >> (16 * (part & 3))) & 0xFFFFu;
+    float y[PASSES][16];
+    float amax = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int row = blk * BM + (warp * PASSES + ps) * 4 + (lane >> 3);
+        float v[16];
+        if (row < N) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (static_cast<size_t>(h) * N + row) * D + 16 * part);
+            const uint4 w0 = src[0], w1 = src[1];
+            const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if ((neg >> i) & 1u) v[i] = -v[i];
+        // index bits 0-3 inside the lane: pairs (i, i + 2^b) for i with bit b clear
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & (1 << b)) continue;
+                const float lo = v[i], hi = v[i + (1 << b)];
+                v[i] = lo + hi;
+                v[i + (1 << b)] = lo - hi;
+            }
+        }
+        // index bits 4-6 = lane bits 0-2: the lane with the bit clear keeps x_i + x_j,
+        // its partner x_i - x_j
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const bool upper = (lane >> k) & 1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float pv = __shfl_xor_sync(0xffffffffu, v[i], 1 << k);
+                v[i] = upper ? pv - v[i] : v[i] + pv;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            y[ps][i] = v[i];
+            if (row < N) amax = fmaxf(amax, fabsf(v[i]));
+        }
+    }
+    __shared__ float red[8];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+    if (threadIdx.x == 0)
+        scales[static_cast<size_t>(h) * nblk + blk] =
+            amax > 0.f ? __fmul_rn(__fdiv_rn(amax, 448.f), 0.0883883476483184f) : 1.f;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int row = blk * BM + (warp * PASSES + ps) * 4 + (lane >> 3);
+        if (row < N) {
+            uint4 out;
+            out.x = ptx::pack_e4m3x4(__fmul_rn(y[ps][0], inv), __fmul_rn(y[ps][1], inv), __fmul_rn(y[ps][2], inv),
+                                     __fmul_rn(y[ps][3], inv));
+            out.y = ptx::pack_e4m3x4(__fmul_rn(y[ps][4], inv), __fmul_rn(y[ps][5], inv), __fmul_rn(y[ps][6], inv),
+                                     __fmul_rn(y[ps][7], inv));
+            out.z = ptx::pack_e4m3x4(__fmul_rn(y[ps][8], inv), __fmul_rn(y[ps][9], inv),
+                                     __fmul_rn(y[ps][10], inv), __fmul_rn(y[ps][11], inv));
+            out.w = ptx::pack_e4m3x4(__fmul_rn(y[ps][12], inv), __fmul_rn(y[ps][13], inv),
+                                     __fmul_rn(y[ps][14], inv), __fmul_rn(y[ps][15], inv));
+            *reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(h) * N + row) * D + 16 * part) = out;
+        }
+    }
+}
+
 // Decode shape, split key sequence: merge the per-split results of each packed query
 // row. With lse_s and o_s (o_s normalised within split s), lse = ln sum_s exp(lse_s)
 // and o = sum_s exp(lse_s - lse) o_s: the log-sum-exp merge of partial softmaxes
@@ -1699,6 +1800,25 @@ int attn_quantize_e4m3(const void *x, void *codes, float *scales, int BH, int N,
     else
         attn::quantize_e4m3_kernel<64><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
                                                              static_cast<uint8_t *>(codes), scales, N, nblk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+int attn_quantize_e4m3_hadamard(const void *x, uint64_t neg_lo, uint64_t neg_hi, void *codes, float *scales,
+                                int BH, int N, int d, void *stream) {
+    if (!x || !codes || !scales) return ATTN_ERR_NULLPTR;
+    if (BH < 1 || N < 1 || N > (1 << 30)) return ATTN_ERR_SHAPE;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (misaligned(x, 16) || misaligned(codes, 16) || misaligned(scales, 4)) return ATTN_ERR_ALIGN;
+    const int nblk = (N + attn::BM - 1) / attn::BM;
+    if (static_cast<long long>(BH) > 65535) return ATTN_ERR_SHAPE;  // grid y
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(BH));
+    attn::quantize_hadamard_e4m3_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                             static_cast<uint8_t *>(codes), scales, N, nblk,
+                                                             static_cast<unsigned long long>(neg_lo),
+                                                             static_cast<unsigned long long>(neg_hi));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;

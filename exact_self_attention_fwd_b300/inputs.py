@@ -118,3 +118,12 @@ def make_dout(B: int, Hq: int, N: int, d: int, seed: int):
     generator seeded with `seed`, rounded to bf16."""
     g = torch.Generator().manual_seed(int(seed))
     return torch.randn((B, Hq, N, d), generator=g, dtype=torch.float32).to(torch.bfloat16).contiguous()
+
+
+def make_signs(d: int, seed: int):
+    """Random signs for incoherent processing: d values, each +1 or -1 with probability
+    1/2, from a generator seeded with `seed` (as fp64 numpy)."""
+    import numpy as np
+    g = torch.Generator().manual_seed(int(seed))
+    bits = torch.randint(0, 2, (d,), generator=g)
+    return np.where(bits.numpy() == 1, -1.0, 1.0)

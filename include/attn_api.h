@@ -157,6 +157,30 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
 int attn_quantize_e4m3(const void *x, void *codes, float *scales, int BH, int N, int d, void *stream);
 
 /*
+ * attn_quantize_e4m3_hadamard -- incoherent processing then block quantisation, as the
+ * FlashAttention-3 review's "Incoherent Processing" describes it for Q and K: each row x
+ * is rotated by the random orthogonal matrix M = diag(s) H / sqrt(d), with s a random
+ * +-1 per channel and H the Hadamard matrix (Sylvester construction, entry (i, j) =
+ * (-1)^popcount(i & j)). The rotated values x M are then block quantised as by
+ * attn_quantize_e4m3. Since M M^T = I, Q' K'^T = Q K^T: quantise Q and K with the same
+ * signs, V with attn_quantize_e4m3, and call attn_fwd_fp8 with the usual scale.
+ *
+ *   x       device, bf16 [BH, N, d], 16-byte aligned (read); d = 128
+ *   neg_lo, neg_hi  the signs: bit c of the 128-bit value (neg_hi:neg_lo) set means
+ *           s_c = -1 (the caller draws them; the same signs for Q and K)
+ *   codes   device, uint8 [BH, N, d], 16-byte aligned (written): e4m3(y * 448 / amax)
+ *           with y = (x o s) H in fp32 and amax the block's largest |y|
+ *   scales  device, fp32 [BH, ceil(N / 128)], 4-byte aligned (written):
+ *           (amax / 448) / sqrt(128) (1 for an all-zero block); code x scale
+ *           approximates the rotated value
+ * y is formed in fp32 by the fast Walsh-Hadamard transform. Its rounding can move a
+ * code that sits within a few fp32 ulps of a rounding boundary to the neighbouring
+ * code. BH <= 65535. ATTN_ERR_UNSUPPORTED for d != 128.
+ */
+int attn_quantize_e4m3_hadamard(const void *x, uint64_t neg_lo, uint64_t neg_hi, void *codes,
+                                float *scales, int BH, int N, int d, void *stream);
+
+/*
  * attn_fwd_fp8 -- the attention forward of attn_fwd on e4m3 operands (the FP8 path of the
  * FlashAttention-3 review): Q, K, V given as codes and block scales from
  * attn_quantize_e4m3; the computed result is attention on the dequantised values.

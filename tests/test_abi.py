@@ -155,3 +155,14 @@ def test_python_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ea.attn_fwd(q, q, q)
+
+
+def test_sign_masks():
+    signs = [1.0] * 128
+    assert ea.sign_masks(signs) == (0, 0)
+    signs[0] = signs[63] = signs[64] = signs[127] = -1.0
+    assert ea.sign_masks(signs) == ((1 << 63) | 1, (1 << 63) | 1)
+    with pytest.raises(ValueError):
+        ea.sign_masks([1.0] * 127)
+    with pytest.raises(ValueError):
+        ea.sign_masks([0.5] * 128)
