@@ -22,7 +22,9 @@
 //                          the result does not depend on the order of the key tiles)
 // Each streamed 128-row tile is taken in two sub-steps of 64 rows (queries in MODE 0,
 // keys in MODE 1), with two tensor-memory buffers for S and dP: the tensor core computes
-// one sub-step's S and dP while the compute warps turn the other's into P and dS.
+// one sub-step's S and dP while the compute warps turn the other's into P and dS. The
+// streamed tiles arrive in 64-row halves through a ring of half-slots, each released as
+// soon as its own sub-step's products have been issued.
 // Warps: 0-3 compute (one tensor-memory row each thread), 4 TMA producer, 5 MMA issuer,
 // 6-7 idle. Tensor memory: sub-step buffer h at [128h, 128h + 128) with S (or S^T) in
 // its first 64 columns and dP in the other 64 (P and dS, bf16, over their first 32),
@@ -48,18 +50,21 @@ struct BwdParams {
 
 template <int D>
 struct BwdCfg {
-    static constexpr int CHUNK_BYTES = BM * 128;  // 64 bf16 columns, 128-byte swizzled
+    static constexpr int CHUNK_BYTES = BM * 128;  // 128 rows x 64 bf16 columns, 128-byte swizzled
     static constexpr int NCHUNK = D / 64;
     static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
-    static constexpr int STAGES = D == 64 ? 4 : 2;              // streamed tile pairs in flight
-    static constexpr int SMEM_FIX = 0;                          // the two stationary tiles
-    static constexpr int SMEM_RING = 2 * TILE_BYTES;            // STAGES x two streamed tiles
-    static constexpr int SMEM_VEC = SMEM_RING + STAGES * 2 * TILE_BYTES;  // per slot: lse2, D
-    static constexpr int SMEM_BAR = SMEM_VEC + STAGES * 2 * BM * 4;
-    static constexpr int B_FIXFULL = 0, B_FIXEMPTY = 1, B_FULL = 2, B_EMPTY = 2 + STAGES;
-    static constexpr int B_SDP = 2 + 2 * STAGES;  // 2: S and dP of sub-step h computed
-    static constexpr int B_PDS = B_SDP + 2;       // 2: P (MODE 0) and dS of sub-step h written (4 warps)
-    static constexpr int B_ACC = B_PDS + 2;       // accumulators of the unit complete
+    static constexpr int HCHUNK_BYTES = CHUNK_BYTES / 2;       // 64 rows x 64 columns
+    static constexpr int HTILE_BYTES = TILE_BYTES / 2;         // 64 rows x d
+    static constexpr int HSTAGES = D == 64 ? 8 : 4;            // streamed half-tile pairs in flight
+    static constexpr int SMEM_FIX = 0;                         // the two stationary tiles
+    static constexpr int SMEM_RING = 2 * TILE_BYTES;           // HSTAGES x two streamed half tiles
+    static constexpr int SMEM_VEC = SMEM_RING + HSTAGES * 2 * HTILE_BYTES;  // per half-slot: lse2, D
+    static constexpr int VEC_BYTES = 2 * 64 * 4;
+    static constexpr int SMEM_BAR = SMEM_VEC + HSTAGES * VEC_BYTES;
+    static constexpr int B_FIXFULL = 0, B_FIXEMPTY = 1, B_FULL = 2, B_EMPTY = 2 + HSTAGES;
+    static constexpr int B_SDP = 2 + 2 * HSTAGES;  // 2: S and dP of sub-step h computed
+    static constexpr int B_PDS = B_SDP + 2;        // 2: P (MODE 0) and dS of sub-step h written (4 warps)
+    static constexpr int B_ACC = B_PDS + 2;        // accumulators of the unit complete
     static constexpr int B_DRAIN = B_ACC + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
@@ -211,10 +216,12 @@ __device__ __forceinline__ BwdUnit bwd_unit(int u, const BwdParams &p) {
     return w;
 }
 
+// tm_fix0, tm_fix1: the stationary operands in 128-row boxes (MODE 0: K, V; MODE 1: Q,
+// dO); tm_str0, tm_str1: the streamed ones in 64-row boxes (MODE 0: Q, dO; MODE 1: K, V)
 template <int D, int MODE>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_fix0, const __grid_constant__ CUtensorMap tm_fix1,
+                    const __grid_constant__ CUtensorMap tm_str0, const __grid_constant__ CUtensorMap tm_str1,
                     const BwdParams p) {
     using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(C::B_FIXFULL), 1);
         ptx::mbar_init(bar(C::B_FIXEMPTY), 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::HSTAGES; ++s) {
             ptx::mbar_init(bar(C::B_FULL + s), 1);
             ptx::mbar_init(bar(C::B_EMPTY + s), 1);
         }
@@ -244,10 +251,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::fence_barrier_init();
     }
     if (warp == BWD_WARP_TMA && lane == 0) {
-        ptx::prefetch_tensormap(&tm_q);
-        ptx::prefetch_tensormap(&tm_k);
-        ptx::prefetch_tensormap(&tm_v);
-        ptx::prefetch_tensormap(&tm_do);
+        ptx::prefetch_tensormap(&tm_fix0);
+        ptx::prefetch_tensormap(&tm_fix1);
+        ptx::prefetch_tensormap(&tm_str0);
+        ptx::prefetch_tensormap(&tm_str1);
     }
     if (warp == BWD_WARP_MMA) {
         ptx::tmem_alloc(sb + C::SMEM_CTL, TMEM_COLS);
@@ -259,16 +266,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t tmem = ctl->tmem_base;
     volatile uint32_t *abort_flag = &ctl->abort;
     const unsigned long long limit = p.timeout_ns;
-    // stationary tiles: MODE 0 holds (K, V), MODE 1 holds (Q, dO); the streamed pair is
-    // (Q, dO) or (K, V)
-    const CUtensorMap *fix0 = MODE == 0 ? &tm_k : &tm_q;
-    const CUtensorMap *fix1 = MODE == 0 ? &tm_v : &tm_do;
-    const CUtensorMap *str0 = MODE == 0 ? &tm_q : &tm_k;
-    const CUtensorMap *str1 = MODE == 0 ? &tm_do : &tm_v;
+    // half-slot n of the ring: streamed operand 0 at half_base(n), operand 1 HTILE_BYTES on
+    auto half_base = [&](uint32_t slot) -> uint32_t { return sb + C::SMEM_RING + slot * 2 * C::HTILE_BYTES; };
 
     if (warp == BWD_WARP_TMA) {
         // ================================================================ producer
-        uint32_t it = 0, fix_it = 0;
+        uint32_t hit = 0, fix_it = 0;
         bool ok = true;
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
@@ -279,9 +282,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_arrive_expect_tx_elect(bar(C::B_FIXFULL), 2 * C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c) {
-                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + c * C::CHUNK_BYTES, fix0, bar(C::B_FIXFULL), c * 64,
+                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + c * C::CHUNK_BYTES, &tm_fix0, bar(C::B_FIXFULL), c * 64,
                                        w.tile * BM, w.zfix);
-                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + C::TILE_BYTES + c * C::CHUNK_BYTES, fix1,
+                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_fix1,
                                        bar(C::B_FIXFULL), c * 64, w.tile * BM, w.zfix);
             }
             for (int s = 0; ok && s < w.steps; ++s) {
@@ -290,35 +293,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const int g = MODE == 0 ? s / n_t : 0;
                 const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
                 const int zs = w.zstream0 + g;
-                const uint32_t slot = it % C::STAGES, ph = ((it / C::STAGES) & 1u) ^ 1u;
-                ok = wait_warp(bar(C::B_EMPTY + slot), ph, abort_flag, limit);
-                if (!ok) break;
-                ++it;
-                const uint32_t dst = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES;
-                if constexpr (MODE == 0) {
-                    // the streamed query tile's lse log2(e) and D (one value per column)
-                    // land beside the tiles on the same barrier
-                    const uint32_t vec = sb + C::SMEM_VEC + slot * 2 * BM * 4;
-                    const size_t idx = static_cast<size_t>(zs) * p.N_pad + t * BM;
-                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES + 2 * BM * 4);
-                    ptx::bulk_load_elect(vec, p.lse2 + idx, BM * 4, bar(C::B_FULL + slot));
-                    ptx::bulk_load_elect(vec + BM * 4, p.dsum + idx, BM * 4, bar(C::B_FULL + slot));
-                } else {
-                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::TILE_BYTES);
-                }
+                for (int h = 0; ok && h < 2; ++h) {
+                    const uint32_t slot = hit % C::HSTAGES, ph = ((hit / C::HSTAGES) & 1u) ^ 1u;
+                    ok = wait_warp(bar(C::B_EMPTY + slot), ph, abort_flag, limit);
+                    if (!ok) break;
+                    ++hit;
+                    const uint32_t dst = half_base(slot);
+                    const int row0 = t * BM + 64 * h;
+                    if constexpr (MODE == 0) {
+                        // the half tile's 64 values of lse log2(e) and of D land beside it
+                        const uint32_t vec = sb + C::SMEM_VEC + slot * C::VEC_BYTES;
+                        const size_t idx = static_cast<size_t>(zs) * p.N_pad + row0;
+                        ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::HTILE_BYTES + C::VEC_BYTES);
+                        ptx::bulk_load_elect(vec, p.lse2 + idx, 64 * 4, bar(C::B_FULL + slot));
+                        ptx::bulk_load_elect(vec + 64 * 4, p.dsum + idx, 64 * 4, bar(C::B_FULL + slot));
+                    } else {
+                        ptx::mbar_arrive_expect_tx_elect(bar(C::B_FULL + slot), 2 * C::HTILE_BYTES);
+                    }
 #pragma unroll
-                for (int c = 0; c < C::NCHUNK; ++c) {
-                    ptx::tma_load_3d_elect(dst + c * C::CHUNK_BYTES, str0, bar(C::B_FULL + slot), c * 64, t * BM, zs);
-                    ptx::tma_load_3d_elect(dst + C::TILE_BYTES + c * C::CHUNK_BYTES, str1, bar(C::B_FULL + slot),
-                                           c * 64, t * BM, zs);
+                    for (int c = 0; c < C::NCHUNK; ++c) {
+                        ptx::tma_load_3d_elect(dst + c * C::HCHUNK_BYTES, &tm_str0, bar(C::B_FULL + slot), c * 64,
+                                               row0, zs);
+                        ptx::tma_load_3d_elect(dst + C::HTILE_BYTES + c * C::HCHUNK_BYTES, &tm_str1,
+                                               bar(C::B_FULL + slot), c * 64, row0, zs);
+                    }
                 }
             }
         }
         if (!ok) {
-            for (uint32_t slot = 0; slot < static_cast<uint32_t>(C::STAGES); ++slot) {
-                if (it <= slot) continue;
-                const uint32_t last = (it - 1u - slot) / C::STAGES * C::STAGES + slot;
-                drain_wait(bar(C::B_FULL + slot), (last / C::STAGES) & 1u, 100000000ull);
+            for (uint32_t slot = 0; slot < static_cast<uint32_t>(C::HSTAGES); ++slot) {
+                if (hit <= slot) continue;
+                const uint32_t last = (hit - 1u - slot) / C::HSTAGES * C::HSTAGES + slot;
+                drain_wait(bar(C::B_FULL + slot), (last / C::HSTAGES) & 1u, 100000000ull);
             }
             if (fix_it) drain_wait(bar(C::B_FIXFULL), (fix_it - 1u) & 1u, 100000000ull);
         }
@@ -329,51 +335,59 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // may overwrite tensor-memory columns that earlier products read.
         constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, 64, false);
         constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(BM, D, true);
-        uint32_t it = 0, fix_use = 0, pds_use0 = 0, pds_use1 = 0;
+        uint32_t hit = 0, fix_use = 0, pds_use0 = 0, pds_use1 = 0;
         bool ok = true;
-        // sub-step h: S (S^T) and dP (dP^T) = A B^T over d, both operands K-major; B is
-        // rows 64h .. 64h + 63 of the streamed tile (8 KB into each 128-row slab)
+        // sub-step h: S (S^T) and dP (dP^T) = A B^T over d, both operands K-major: A the
+        // stationary 128-row tile, B the streamed 64-row half tile
         auto issue_sdp = [&](int h, uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
             const uint32_t col = C::COL_BUF * h;
             const uint64_t a0d = ptx::sdesc_sw128(a0, 16, 1024), a1d = ptx::sdesc_sw128(a1, 16, 1024);
-            const uint64_t b0d = ptx::sdesc_sw128(b0 + h * 8192, 16, 1024);
-            const uint64_t b1d = ptx::sdesc_sw128(b1 + h * 8192, 16, 1024);
+            const uint64_t b0d = ptx::sdesc_sw128(b0, 16, 1024), b1d = ptx::sdesc_sw128(b1, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_elect(tmem + col + C::COL_S, a0d + off, b0d + off, IDESC_S, kk > 0 ? 1u : 0u);
+                const uint32_t aoff = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                const uint32_t boff = ((kk >> 2) * C::HCHUNK_BYTES + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_elect(tmem + col + C::COL_S, a0d + aoff, b0d + boff, IDESC_S, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_elect(tmem + col + C::COL_DP, a1d + off, b1d + off, IDESC_S, kk > 0 ? 1u : 0u);
+                const uint32_t aoff = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                const uint32_t boff = ((kk >> 2) * C::HCHUNK_BYTES + (kk & 3) * 32) >> 4;
+                ptx::mma_ss_elect(tmem + col + C::COL_DP, a1d + aoff, b1d + boff, IDESC_S, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit_elect(bar(C::B_SDP + h));
         };
-        // D[tmem] (+)= A[tmem, bf16] B for sub-step h: A = 64 packed rows' worth of P / dS
-        // (32 columns), B = rows 64h .. 64h + 63 of a [128 x d] tile read MN-major
-        auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, int h, bool accumulate) {
-            const uint64_t bd = ptx::sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+        // D[tmem] (+)= A[tmem, bf16] B for one sub-step: A = 64 rows' worth of P / dS (32
+        // packed columns), B = a streamed [64 x d] half tile read MN-major
+        auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, bool accumulate) {
+            const uint64_t bd = ptx::sdesc_sw128(b_addr, C::HCHUNK_BYTES, 1024);
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int kr = 4 * h + k4;  // 16-row step within the tile
-                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + k4 * 8, bd + ((kr * 2048) >> 4), IDESC_ACC,
+            for (int k4 = 0; k4 < 4; ++k4)
+                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + k4 * 8, bd + ((k4 * 2048) >> 4), IDESC_ACC,
                                   (accumulate || k4 > 0) ? 1u : 0u);
-            }
         };
-        // the accumulating products of sub-step h, once the compute warps wrote P / dS
-        auto issue_products = [&](int h, uint32_t s0, uint32_t s1, bool accumulate) -> bool {
+        // the accumulating products of sub-step h (half tile at hb), once the compute warps
+        // wrote its P / dS
+        auto issue_products = [&](int h, uint32_t hb, bool accumulate) -> bool {
             uint32_t &use = h ? pds_use1 : pds_use0;
             if (!wait_warp(bar(C::B_PDS + h), use & 1u, abort_flag, limit)) return false;
             ++use;
             ptx::tc_fence_after();
             const uint32_t buf = C::COL_BUF * h;
             if constexpr (MODE == 0) {
-                issue_acc(C::COL_A0, buf + C::COL_S, s1, h, accumulate);   // dV += P^T dO
-                issue_acc(C::COL_A1, buf + C::COL_DP, s0, h, accumulate);  // dK += dS^T Q
+                issue_acc(C::COL_A0, buf + C::COL_S, hb + C::HTILE_BYTES, accumulate);  // dV += P^T dO
+                issue_acc(C::COL_A1, buf + C::COL_DP, hb, accumulate);                 // dK += dS^T Q
             } else {
-                issue_acc(C::COL_A0, buf + C::COL_S, s0, h, accumulate);   // dQ += dS K
+                issue_acc(C::COL_A0, buf + C::COL_S, hb, accumulate);                  // dQ += dS K
             }
+            return true;
+        };
+        auto next_half = [&](uint32_t &slot) -> bool {
+            slot = hit % C::HSTAGES;
+            const uint32_t ph = (hit / C::HSTAGES) & 1u;
+            ++hit;
+            if (!wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit)) return false;
+            ptx::tc_fence_after();
             return true;
         };
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
@@ -384,31 +398,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t f0 = sb + C::SMEM_FIX, f1 = sb + C::SMEM_FIX + C::TILE_BYTES;
-            uint32_t prev_s0 = 0, prev_s1 = 0, prev_slot = 0;
+            uint32_t prev_slot = 0;
             for (int s = 0; s < w.steps; ++s) {
-                const uint32_t slot = it % C::STAGES, ph = (it / C::STAGES) & 1u;
-                ++it;
-                ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                const uint32_t s0 = sb + C::SMEM_RING + slot * 2 * C::TILE_BYTES, s1 = s0 + C::TILE_BYTES;
                 // order: S, dP of (s, 0); products of (s - 1, 1); S, dP of (s, 1); products
                 // of (s, 0). Buffer h is rewritten only after the products that read its P
                 // and dS were issued, and the tensor core always has the next sub-step's
-                // S and dP to compute while the compute warps work.
-                issue_sdp(0, f0, f1, s0, s1);
+                // S and dP to compute while the compute warps work. A half-slot is
+                // released right after its sub-step's products.
+                uint32_t slot0, slot1;
+                if (!(ok = next_half(slot0))) break;
+                issue_sdp(0, f0, f1, half_base(slot0), half_base(slot0) + C::HTILE_BYTES);
                 if (s > 0) {
-                    if (!(ok = issue_products(1, prev_s0, prev_s1, true))) break;
+                    if (!(ok = issue_products(1, half_base(prev_slot), true))) break;
                     ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
                 }
-                issue_sdp(1, f0, f1, s0, s1);
-                if (!(ok = issue_products(0, s0, s1, s > 0))) break;
-                prev_s0 = s0;
-                prev_s1 = s1;
-                prev_slot = slot;
+                if (!(ok = next_half(slot1))) break;
+                issue_sdp(1, f0, f1, half_base(slot1), half_base(slot1) + C::HTILE_BYTES);
+                if (!(ok = issue_products(0, half_base(slot0), s > 0))) break;
+                ptx::mma_commit_elect(bar(C::B_EMPTY + slot0));
+                prev_slot = slot1;
             }
             if (!ok) break;
-            if (!(ok = issue_products(1, prev_s0, prev_s1, true))) break;
+            if (!(ok = issue_products(1, half_base(prev_slot), true))) break;
             ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
             ptx::mma_commit_elect(bar(C::B_FIXEMPTY));
             ptx::mma_commit_elect(bar(C::B_ACC));
@@ -420,7 +431,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // ================================================================ compute
         const int row = warp * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        uint32_t it = 0, sdp_use0 = 0, sdp_use1 = 0, acc_use = 0;
+        uint32_t hit = 0, sdp_use0 = 0, sdp_use1 = 0, acc_use = 0;
         bool ok = true;
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
@@ -443,14 +454,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const int n_t = w.hi - w.lo;
                 const int g = MODE == 0 ? s / n_t : 0;
                 const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
-                const uint32_t slot = it % C::STAGES, ph = (it / C::STAGES) & 1u;
-                ++it;
-                const float *vec = reinterpret_cast<const float *>(smem + C::SMEM_VEC) + slot * 2 * BM;
-                if constexpr (MODE == 0) {
-                    // the per-column lse and D were staged with the tiles of this slot
-                    ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
-                    if (!ok) break;
-                }
                 (void)g;
                 // columns of this tile the row sees: [c_lo, c_hi] relative to the tile
                 const int c0 = t * BN;
@@ -461,6 +464,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
+                    const uint32_t slot = hit % C::HSTAGES, ph = (hit / C::HSTAGES) & 1u;
+                    ++hit;
+                    const float *vec = reinterpret_cast<const float *>(smem + C::SMEM_VEC + slot * C::VEC_BYTES);
+                    if constexpr (MODE == 0) {
+                        // the half tile's lse and D were staged with it
+                        ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
+                        if (!ok) break;
+                    }
                     // sub-step h: columns 64h .. 64h + 63 of the tile
                     const bool covers = !none && c_lo <= 64 * h && c_hi >= 64 * h + 63;
                     const bool need_mask = !__all_sync(0xffffffffu, covers);
@@ -483,8 +494,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                         for (int e4 = 0; e4 < 8; ++e4) {
                             float4 l4, d4;
                             if constexpr (MODE == 0) {
-                                l4 = *reinterpret_cast<const float4 *>(vec + cb + 4 * e4);
-                                d4 = *reinterpret_cast<const float4 *>(vec + BM + cb + 4 * e4);
+                                l4 = *reinterpret_cast<const float4 *>(vec + 32 * c + 4 * e4);
+                                d4 = *reinterpret_cast<const float4 *>(vec + 64 + 32 * c + 4 * e4);
                             } else {
                                 l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
                                 d4 = make_float4(row_d, row_d, row_d, row_d);

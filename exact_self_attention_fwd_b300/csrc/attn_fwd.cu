@@ -1357,12 +1357,14 @@ int encode_map_u8(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, 
     return ATTN_OK;
 }
 
-int encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int N, long long BH) {
+// bf16 [BH, N, d] as boxes of `rows` rows x 64 columns (128 bytes), 128-byte swizzled
+int encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int N, long long BH,
+               int rows = attn::BM) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
                              static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
-    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(attn::BM), 1u};
+    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(rows), 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1647,12 +1649,17 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
     const long long BHq = static_cast<long long>(B) * Hq, BHkv = static_cast<long long>(B) * Hkv;
-    CUtensorMap mq, mk, mv, mdo;
+    // 128-row boxes for the stationary operands, 64-row boxes for the streamed ones
+    CUtensorMap mq, mk, mv, mdo, mq64, mk64, mv64, mdo64;
     int rc;
     if ((rc = encode_map(enc, &mq, q, D, N, BHq)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mk, k, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, N, BHkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mdo, dout, D, N, BHq)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mq64, q, D, N, BHq, 64)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mk64, k, D, N, BHkv, 64)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mv64, v, D, N, BHkv, 64)) != ATTN_OK) return rc;
+    if ((rc = encode_map(enc, &mdo64, dout, D, N, BHq, 64)) != ATTN_OK) return rc;
     const int n_pad = static_cast<int>(bwd_n_pad(N));
     float *lse2 = static_cast<float *>(workspace);
     float *dsum = lse2 + BHq * n_pad;
@@ -1691,14 +1698,14 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     // dK, dV: one unit per (key tile, batch, kv head)
     p.num_units = static_cast<int>(BHkv * p.n_kv);
     int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_bwd_kernel<D, 0><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv,
-                                                                                                  mdo, p);
+    attn::attn_bwd_kernel<D, 0><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mk, mv, mq64,
+                                                                                                  mdo64, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     // dQ: one unit per (query tile, batch, query head)
     p.num_units = static_cast<int>(BHq * p.n_kv);
     grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_bwd_kernel<D, 1><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv,
-                                                                                                  mdo, p);
+    attn::attn_bwd_kernel<D, 1><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mdo, mk64,
+                                                                                                  mv64, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }
