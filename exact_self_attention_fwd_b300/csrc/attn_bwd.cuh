@@ -25,15 +25,16 @@
 // one sub-step's S and dP while the compute warps turn the other's into P and dS. The
 // streamed tiles arrive in 64-row halves through a ring of half-slots, each released as
 // soon as its own sub-step's products have been issued.
-// Warps: 0-3 compute (one tensor-memory row each thread), 4 TMA producer, 5 MMA issuer,
-// 6-7 idle. Tensor memory: sub-step buffer h at [128h, 128h + 128) with S (or S^T) in
+// Warps: 0-3 compute the first sub-step of every tile and 4-7 the second (one tensor-
+// memory row each thread, so the two run side by side on one tile), 8 TMA producer, 9
+// MMA issuer. Tensor memory: sub-step buffer h at [128h, 128h + 128) with S (or S^T) in
 // its first 64 columns and dP in the other 64 (P and dS, bf16, over their first 32),
 // then the accumulators from column 256.
 #pragma once
 
-constexpr int BWD_THREADS = 256;
-constexpr int BWD_WARP_TMA = 4;
-constexpr int BWD_WARP_MMA = 5;
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_WARP_TMA = 8;
+constexpr int BWD_WARP_MMA = 9;
 
 struct BwdParams {
     const float *lse2;  // lse log2(e) per query row, fp32 [B * Hq * N_pad] (0 past N)
@@ -65,7 +66,8 @@ struct BwdCfg {
     static constexpr int B_SDP = 2 + 2 * HSTAGES;  // 2: S and dP of sub-step h computed
     static constexpr int B_PDS = B_SDP + 2;        // 2: P (MODE 0) and dS of sub-step h written (4 warps)
     static constexpr int B_ACC = B_PDS + 2;        // accumulators of the unit complete
-    static constexpr int B_DRAIN = B_ACC + 1;
+    static constexpr int B_AFREE = B_ACC + 1;      // accumulators read by the epilogue (8 warps)
+    static constexpr int B_DRAIN = B_AFREE + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_ALLOC = SMEM_CTL + 16 + 1024;
@@ -246,6 +248,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_init(bar(C::B_PDS + h), 4);
         }
         ptx::mbar_init(bar(C::B_ACC), 1);
+        ptx::mbar_init(bar(C::B_AFREE), 8);
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
         ptx::fence_barrier_init();
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // may overwrite tensor-memory columns that earlier products read.
         constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, 64, false);
         constexpr uint32_t IDESC_ACC = ptx::idesc_bf16_f32(BM, D, true);
-        uint32_t hit = 0, fix_use = 0, pds_use0 = 0, pds_use1 = 0;
+        uint32_t hit = 0, fix_use = 0, pds_use0 = 0, pds_use1 = 0, acc_fills = 0;
         bool ok = true;
         // sub-step h: S (S^T) and dP (dP^T) = A B^T over d, both operands K-major: A the
         // stationary 128-row tile, B the streamed 64-row half tile
@@ -414,6 +417,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 }
                 if (!(ok = next_half(slot1))) break;
                 issue_sdp(1, f0, f1, half_base(slot1), half_base(slot1) + C::HTILE_BYTES);
+                if (s == 0) {
+                    // the unit's first products overwrite the accumulators: both compute
+                    // warpgroups must have read the previous unit's (a fresh barrier
+                    // passes parity 1)
+                    ok = wait_warp(bar(C::B_AFREE), (acc_fills & 1u) ^ 1u, abort_flag, limit);
+                    ++acc_fills;
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                }
                 if (!(ok = issue_products(0, half_base(slot0), s > 0))) break;
                 ptx::mma_commit_elect(bar(C::B_EMPTY + slot0));
                 prev_slot = slot1;
@@ -427,11 +439,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::mma_commit_elect(bar(C::B_DRAIN));
         drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ================================================================ compute
-        const int row = warp * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        uint32_t hit = 0, sdp_use0 = 0, sdp_use1 = 0, acc_use = 0;
+        // warpgroup h (warps 4h .. 4h + 3) takes sub-step h of every tile
+        const int h = warp >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + C::COL_BUF * h + C::COL_S;
+        const uint32_t t_dp = tmem + lane_off + C::COL_BUF * h + C::COL_DP;
+        uint32_t hit = 0, sdp_use = 0, acc_use = 0;
         bool ok = true;
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
@@ -455,83 +472,79 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const int g = MODE == 0 ? s / n_t : 0;
                 const int t = w.lo + (MODE == 0 ? s - g * n_t : s);
                 (void)g;
-                // columns of this tile the row sees: [c_lo, c_hi] relative to the tile
+                // half-slot of this sub-step: the tile's two halves take consecutive slots
+                const uint32_t slot = (hit + h) % C::HSTAGES, ph = ((hit + h) / C::HSTAGES) & 1u;
+                hit += 2;
+                const float *vec = reinterpret_cast<const float *>(smem + C::SMEM_VEC + slot * C::VEC_BYTES);
+                if constexpr (MODE == 0) {
+                    // the half tile's lse and D were staged with it
+                    ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
+                    if (!ok) break;
+                }
+                // columns 64h .. 64h + 63 of the tile; those this row sees: [c_lo, c_hi]
                 const int c0 = t * BN;
                 const int c_hi = min(ihi, c0 + BN - 1) - c0;
                 const int c_lo = max(ilo, c0) - c0;
                 const bool none = c_hi < c_lo;
                 const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
                 const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
+                const bool covers = !none && c_lo <= 64 * h && c_hi >= 64 * h + 63;
+                const bool need_mask = !__all_sync(0xffffffffu, covers);
+                ok = wait_warp(bar(C::B_SDP + h), sdp_use & 1u, abort_flag, limit);
+                ++sdp_use;
+                if (!ok) break;
+                ptx::tc_fence_after();
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t slot = hit % C::HSTAGES, ph = (hit / C::HSTAGES) & 1u;
-                    ++hit;
-                    const float *vec = reinterpret_cast<const float *>(smem + C::SMEM_VEC + slot * C::VEC_BYTES);
-                    if constexpr (MODE == 0) {
-                        // the half tile's lse and D were staged with it
-                        ok = wait_warp(bar(C::B_FULL + slot), ph, abort_flag, limit);
-                        if (!ok) break;
-                    }
-                    // sub-step h: columns 64h .. 64h + 63 of the tile
-                    const bool covers = !none && c_lo <= 64 * h && c_hi >= 64 * h + 63;
-                    const bool need_mask = !__all_sync(0xffffffffu, covers);
-                    uint32_t &use = h ? sdp_use1 : sdp_use0;
-                    ok = wait_warp(bar(C::B_SDP + h), use & 1u, abort_flag, limit);
-                    ++use;
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    const uint32_t t_s = tmem + lane_off + C::COL_BUF * h + C::COL_S;
-                    const uint32_t t_dp = tmem + lane_off + C::COL_BUF * h + C::COL_DP;
-#pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t sr[32], dr[32];
-                        ptx::tmem_ld32(t_s + 32 * c, sr);
-                        ptx::tmem_ld32(t_dp + 32 * c, dr);
-                        const int cb = 64 * h + 32 * c;  // first column of the chunk in the tile
-                        ptx::tmem_wait_ld();
-                        uint32_t pk[16], dk16[16];
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sr[32], dr[32];
+                    ptx::tmem_ld32(t_s + 32 * c, sr);
+                    ptx::tmem_ld32(t_dp + 32 * c, dr);
+                    const int cb = 64 * h + 32 * c;  // first column of the chunk in the tile
+                    ptx::tmem_wait_ld();
+                    uint32_t pk[16], dk16[16];
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            float4 l4, d4;
-                            if constexpr (MODE == 0) {
-                                l4 = *reinterpret_cast<const float4 *>(vec + 32 * c + 4 * e4);
-                                d4 = *reinterpret_cast<const float4 *>(vec + 64 + 32 * c + 4 * e4);
-                            } else {
-                                l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
-                                d4 = make_float4(row_d, row_d, row_d, row_d);
-                            }
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                            float pp[4], ds[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int e = 4 * e4 + q;
-                                float pv = ptx::ex2(fmaf(__uint_as_float(sr[e]), p.sl2, -lv[q]));
-                                if (need_mask && static_cast<uint32_t>(cb + e) - base > span) pv = 0.f;
-                                pp[q] = pv;
-                                ds[q] = pv * (__uint_as_float(dr[e]) - dv[q]);
-                            }
-                            pk[2 * e4] = ptx::pack_bf16x2(pp[0], pp[1]);
-                            pk[2 * e4 + 1] = ptx::pack_bf16x2(pp[2], pp[3]);
-                            dk16[2 * e4] = ptx::pack_bf16x2(ds[0], ds[1]);
-                            dk16[2 * e4 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
-                        }
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        float4 l4, d4;
                         if constexpr (MODE == 0) {
-                            ptx::tmem_st16(t_s + 16 * c, pk);     // P^T, A of dV += P^T dO
-                            ptx::tmem_st16(t_dp + 16 * c, dk16);  // dS^T, A of dK += dS^T Q
+                            l4 = *reinterpret_cast<const float4 *>(vec + 32 * c + 4 * e4);
+                            d4 = *reinterpret_cast<const float4 *>(vec + 64 + 32 * c + 4 * e4);
                         } else {
-                            ptx::tmem_st16(t_s + 16 * c, dk16);   // dS, A of dQ += dS K
+                            l4 = make_float4(row_lse2, row_lse2, row_lse2, row_lse2);
+                            d4 = make_float4(row_d, row_d, row_d, row_d);
                         }
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pp[4], ds[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = 4 * e4 + q;
+                            float pv = ptx::ex2(fmaf(__uint_as_float(sr[e]), p.sl2, -lv[q]));
+                            if (need_mask && static_cast<uint32_t>(cb + e) - base > span) pv = 0.f;
+                            pp[q] = pv;
+                            ds[q] = pv * (__uint_as_float(dr[e]) - dv[q]);
+                        }
+                        pk[2 * e4] = ptx::pack_bf16x2(pp[0], pp[1]);
+                        pk[2 * e4 + 1] = ptx::pack_bf16x2(pp[2], pp[3]);
+                        dk16[2 * e4] = ptx::pack_bf16x2(ds[0], ds[1]);
+                        dk16[2 * e4 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
                     }
-                    ptx::tmem_wait_st();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS + h));
+                    if constexpr (MODE == 0) {
+                        ptx::tmem_st16(t_s + 16 * c, pk);     // P^T, A of dV += P^T dO
+                        ptx::tmem_st16(t_dp + 16 * c, dk16);  // dS^T, A of dK += dS^T Q
+                    } else {
+                        ptx::tmem_st16(t_s + 16 * c, dk16);   // dS, A of dQ += dS K
+                    }
                 }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS + h));
             }
             if (!ok) break;
-            // epilogue: MODE 0 writes dV and scale * dK of the key rows, MODE 1 scale * dQ;
-            // a unit with nothing to stream writes zeros
+            // epilogue, split between the warpgroups: MODE 0 writes dV (warpgroup 0) and
+            // scale * dK (warpgroup 1) of the key rows; MODE 1 writes scale * dQ, columns
+            // [0, d/2) from warpgroup 0 and [d/2, d) from warpgroup 1. A unit with nothing
+            // to stream writes zeros.
             const bool has = w.steps > 0;
             if (has) {
                 ok = wait_warp(bar(C::B_ACC), acc_use & 1u, abort_flag, limit);
@@ -539,42 +552,45 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
             }
+            __nv_bfloat16 *out = MODE == 0 ? (h == 0 ? p.dv : p.dk) : p.dq;
+            const float mul = (MODE == 0 && h == 0) ? 1.f : p.scale;
+            constexpr int NC = MODE == 0 ? D / 32 : D / 64;  // 32-column chunks this warpgroup writes
+            const int col0 = MODE == 0 ? 0 : h * (D / 2);
+            const uint32_t t_acc = tmem + lane_off + (MODE == 0 ? (h == 0 ? C::COL_A0 : C::COL_A1) : C::COL_A0) + col0;
 #pragma unroll 1
-            for (int a = 0; a < (MODE == 0 ? 2 : 1); ++a) {
-                __nv_bfloat16 *out = MODE == 0 ? (a == 0 ? p.dv : p.dk) : p.dq;
-                const float mul = (MODE == 0 && a == 0) ? 1.f : p.scale;
-                const uint32_t t_acc = tmem + lane_off + (a == 0 ? C::COL_A0 : C::COL_A1);
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    if (has) {
-                        ptx::tmem_ld32(t_acc + 32 * c, r);
-                        ptx::tmem_wait_ld();
-                    } else {
+            for (int c = 0; c < NC; ++c) {
+                uint32_t r[32];
+                if (has) {
+                    ptx::tmem_ld32(t_acc + 32 * c, r);
+                    ptx::tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = 0u;
-                    }
-                    if (r_abs < p.N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(w.zfix) * p.N + r_abs) * D +
-                                                               32 * c);
+                    for (int e = 0; e < 32; ++e) r[e] = 0u;
+                }
+                if (r_abs < p.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(w.zfix) * p.N + r_abs) * D + col0 +
+                                                           32 * c);
 #pragma unroll
-                        for (int g4 = 0; g4 < 4; ++g4) {
-                            uint4 val;
-                            val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 0]) * mul,
-                                                     __uint_as_float(r[8 * g4 + 1]) * mul);
-                            val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * mul,
-                                                     __uint_as_float(r[8 * g4 + 3]) * mul);
-                            val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * mul,
-                                                     __uint_as_float(r[8 * g4 + 5]) * mul);
-                            val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * mul,
-                                                     __uint_as_float(r[8 * g4 + 7]) * mul);
-                            dst[g4] = val;
-                        }
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        uint4 val;
+                        val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 0]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 1]) * mul);
+                        val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 3]) * mul);
+                        val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 5]) * mul);
+                        val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 7]) * mul);
+                        dst[g4] = val;
                     }
                 }
             }
-            // the accumulators are read: the next unit's first products overwrite them
-            ptx::tc_fence_before();
+            if (has) {
+                // the accumulators are read: the next unit's first products may overwrite them
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_AFREE));
+            }
         }
     }
     ptx::tc_fence_before();
