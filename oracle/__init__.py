@@ -82,6 +82,10 @@ def _declare(lib):
     lib.attn_ref_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                      ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p]
     lib.attn_ref_bwd_f64.restype = ctypes.c_int
+    lib.attn_ref_bwd_dq_rows_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
+                                             ctypes.c_double, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.POINTER(ctypes.c_int64), i64, f64p]
+    lib.attn_ref_bwd_dq_rows_f64.restype = ctypes.c_int
     lib.attn_ref_quantize_e4m3_blocks_f64.argtypes = [f64p, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_uint8),
                                                       f64p]
     lib.attn_ref_quantize_e4m3_blocks_f64.restype = ctypes.c_int
@@ -275,6 +279,30 @@ def attn_ref_f64in(q, k, v, causal: bool = False, window: int = 0, scale: float 
     if rows_arr is None:
         return o.reshape(B, Hq, N, d), lse.reshape(B, Hq, N)
     return o, lse
+
+
+def attn_ref_bwd_dq_rows(q, k, v, do, rows, causal: bool = False, window: int = 0,
+                         scale: float | None = None, key_len=None, lib=None):
+    """fp64 query gradients [len(rows), d] of the flat query rows (b * Hq + hq) * N + i,
+    each computed from its own row (the exact row term D), for full-size checks."""
+    qb, kb, vb, db = (_as_bits(t) for t in (q, k, v, do))
+    B, Hq, N, d = qb.shape
+    Hkv = kb.shape[1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.empty((len(r), d), dtype=np.float64)
+    kl = None if key_len is None else np.ascontiguousarray(np.asarray(key_len, dtype=np.int32))
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    rc = (lib or load()).attn_ref_bwd_dq_rows_f64(
+        qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
+        B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
+        kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
+        r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(r),
+        out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
 
 
 def hadamard(d: int) -> np.ndarray:

@@ -497,6 +497,81 @@ int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, co
     return bwd_core(q, k, v, do_, NULL, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv);
 }
 
+/*
+ * The query gradient of selected rows, each from its own row of the definition (the
+ * backward above restricted to dq): for flat query row r = (b * Hq + hq) * N + i,
+ * p_ij and dp_ij over the keys row i sees, D_i = sum_j p_ij dp_ij, and
+ * dq_i = scale sum_j p_ij (dp_ij - D_i) k_j. Writes dq [nrows, d] (fp64). Cost O(N d)
+ * per row, so rows of full-size problems can be checked one by one.
+ */
+int attn_ref_bwd_dq_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                             int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int causal,
+                             int64_t window, double scale, const int32_t *key_len, const int64_t *rows,
+                             int64_t nrows, double *dq) {
+    if (!q || !k || !v || !do_ || !rows || !dq || nrows < 0) return -1;
+    int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc) return rc;
+    const int64_t group = Hq / Hkv;
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!p || !dp) {
+        free(p);
+        free(dp);
+        return -5;
+    }
+    for (int64_t n = 0; n < nrows; ++n) {
+        const int64_t r = rows[n];
+        double *out = dq + n * d;
+        for (int64_t c = 0; c < d; ++c) out[c] = 0.0;
+        if (r < 0 || r >= B * Hq * N) {
+            free(p);
+            free(dp);
+            return -2;
+        }
+        const int64_t bh = r / N, i = r % N, b = bh / Hq, hq = bh % Hq, kv = hq / group;
+        int64_t L = key_len ? (int64_t)key_len[b] : N;
+        if (L < 0) L = 0;
+        if (L > N) L = N;
+        const uint16_t *qi = q + r * d, *doi = do_ + r * d;
+        const uint16_t *kh = k + (b * Hkv + kv) * N * d, *vh = v + (b * Hkv + kv) * N * d;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            p[j] = 0.0;
+            if (!key_visible(i, j, causal, window, L)) continue;
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += bf16_bits_to_double(qi[c]) * bf16_bits_to_double(kh[j * d + c]);
+            p[j] = scale * dot;
+            if (p[j] > m) m = p[j];
+        }
+        if (m == -INFINITY) continue; /* no visible key: dq = 0 */
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            if (key_visible(i, j, causal, window, L)) l += exp(p[j] - m);
+        const double lse = m + log(l);
+        double dsum = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            dp[j] = 0.0;
+            if (!key_visible(i, j, causal, window, L)) {
+                p[j] = 0.0;
+                continue;
+            }
+            p[j] = exp(p[j] - lse);
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c) dot += bf16_bits_to_double(doi[c]) * bf16_bits_to_double(vh[j * d + c]);
+            dp[j] = dot;
+            dsum += p[j] * dp[j];
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0) continue;
+            const double ds = p[j] * (dp[j] - dsum);
+            for (int64_t c = 0; c < d; ++c) out[c] += scale * ds * bf16_bits_to_double(kh[j * d + c]);
+        }
+    }
+    free(p);
+    free(dp);
+    return 0;
+}
+
 int attn_ref_bwd_given_o_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
                              const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
                              int causal, int64_t window, double scale, const int32_t *key_len,

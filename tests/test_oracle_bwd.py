@@ -228,3 +228,20 @@ def test_bwd_pins_catch_mutant(name, tmp_path):
     worst = max(np.abs(dq - qt.grad.numpy()).max(), np.abs(dk - kt.grad.numpy()).max(),
                 np.abs(dv - vt.grad.numpy()).max())
     assert worst > 1e-6, f"mutant {name} not caught"
+
+
+def test_dq_rows_match_full_backward():
+    # the row-by-row query gradient equals the full backward's, for every row, with and
+    # without padding, window and grouped heads
+    g = torch.Generator().manual_seed(60)
+    B, Hq, Hkv, N, d = 2, 4, 2, 45, 16
+    q = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    k, v = (torch.randn(B, Hkv, N, d, generator=g).bfloat16() for _ in range(2))
+    do = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    rows = np.arange(B * Hq * N)
+    for causal, W, kl in ((True, 0, None), (False, 7, [45, 20]), (True, 11, [30, 45])):
+        dq, _, _ = oracle.attn_ref_bwd(q, k, v, do, causal=causal, window=W, scale=0.3, key_len=kl)
+        dq_rows = oracle.attn_ref_bwd_dq_rows(q, k, v, do, rows, causal=causal, window=W, scale=0.3, key_len=kl)
+        np.testing.assert_allclose(dq_rows, dq.reshape(-1, d), atol=1e-12, rtol=0)
+    with pytest.raises(ValueError):
+        oracle.attn_ref_bwd_dq_rows(q, k, v, do, [B * Hq * N], causal=True, scale=0.3)
