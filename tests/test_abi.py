@@ -166,3 +166,39 @@ def test_sign_masks():
         ea.sign_masks([1.0] * 127)
     with pytest.raises(ValueError):
         ea.sign_masks([0.5] * 128)
+
+
+def test_backward_entry_validates(lib):
+    # q, k, v, o, lse, dout, dq, dk, dv, key_len, B, Hq, Hkv, N, d, causal, window, scale,
+    # workspace, workspace_bytes, stream
+    need = lib.attn_bwd_workspace_size(1, 2, 300, 128)
+    # (lse log2(e), D) per row, rows padded to 384
+    assert need == 2 * 1 * 2 * 384 * 4
+    assert lib.attn_bwd_workspace_size(1, 2, 300, 96) == 0
+    args = [A] * 9 + [None, 1, 2, 1, 300, 128, 1, 0, 0.1, A, need, None]
+    for i in (0, 5, 6, 7, 8, 18):
+        bad = list(args)
+        bad[i] = None
+        assert lib.attn_bwd(*bad) == ea.ATTN_ERR_NULLPTR, i
+    bad = list(args)
+    bad[14] = 96
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[12] = 3                                   # Hq not a multiple of Hkv
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_SHAPE
+    bad = list(args)
+    bad[6] = A + 8                                # dq not 16-byte aligned
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_ALIGN
+    bad = list(args)
+    bad[18] = A + 16                              # workspace not 256-byte aligned
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_ALIGN
+    bad = list(args)
+    bad[19] = need - 4
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_WORKSPACE
+
+
+def test_hadamard_quantiser_validates(lib):
+    assert lib.attn_quantize_e4m3_hadamard(None, 0, 0, A, A, 1, 128, 128, None) == ea.ATTN_ERR_NULLPTR
+    assert lib.attn_quantize_e4m3_hadamard(A, 0, 0, A, A, 1, 128, 64, None) == ea.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_quantize_e4m3_hadamard(A, 0, 0, A + 8, A, 1, 128, 128, None) == ea.ATTN_ERR_ALIGN
+    assert lib.attn_quantize_e4m3_hadamard(A, 0, 0, A, A, 70000, 128, 128, None) == ea.ATTN_ERR_SHAPE
