@@ -364,7 +364,7 @@ def roofline_of(w: Workload, seconds_per_call: float, peaks: dict) -> dict:
             "frac_vs_sustained": achieved / sustained}
 
 
-def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0):
+def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset: int = 0, flush: bool = True):
     """Device time per attn_fwd call on workload w (seconds).
 
     Calls of at least a few microseconds are timed one by one with CUDA events, a
@@ -402,18 +402,20 @@ def measure_workload(ea, w: Workload, dev, steps: int, warmup: int, seed_offset:
         torch.cuda.synchronize(dev)
         per = s0.elapsed_time(s1) / 1e3 / steps
         return per, "CUDA graph of %d calls" % steps
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for i in range(steps):
-            flush_l2(flush)
+            if flush:
+                flush_l2(buf)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
     torch.cuda.synchronize(dev)
     per = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3 / steps
-    return per, "per-call CUDA events, L2 flushed between calls"
+    return per, ("per-call CUDA events, L2 flushed between calls" if flush
+                 else "per-call CUDA events, calls back to back (no flush)")
 
 
 def measure_decode(ea, w: DecodeWorkload, dev, steps: int, warmup: int, seed_offset: int = 0):
@@ -692,6 +694,12 @@ def run_ours(args, w: Workload):
             summary[name] = {"tflops": flops(ww) / t_call / 1e12, "us_per_call": t_call * 1e6,
                              "gbs": hbm_bytes(ww) / t_call / 1e9, "bound": r["bound"],
                              "frac": r["frac"], "timing": how}
+            if name in ("vit_base", "gpt2_small"):
+                # the short-sequence workloads are also reported without the flush
+                t_nf, _ = measure_workload(ea, ww, dev, args.summary_steps, 5, seed_offset=rank, flush=False)
+                summary[name].update({"us_per_call_no_flush": t_nf * 1e6,
+                                      "tflops_no_flush": flops(ww) / t_nf / 1e12,
+                                      "gbs_no_flush": hbm_bytes(ww) / t_nf / 1e9})
         fw = WORKLOADS["gqa_8k"]
         t_attn, t_quant, t_quant_h = measure_fp8(ea, fw, dev, args.summary_steps, 5, seed_offset=rank)
         fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
