@@ -139,11 +139,7 @@ struct Cfg {
     static constexpr int Q_BUFS = (D == 64 || F8) ? 2 : 1;
     static constexpr int SMEM_Q = 0;
     static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
-    // one 64-column staging block per softmax warpgroup: O (bf16) goes registers -> shared
-    // memory (128-byte-swizzled, like the TMA loads) -> global by a TMA tensor store
-    static constexpr int STAGE_BYTES = BM * 64 * 2;
-    static constexpr int SMEM_STAGE = SMEM_KV + STAGES * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_STAGE + 2 * STAGE_BYTES;
+    static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
     static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
@@ -154,9 +150,7 @@ struct Cfg {
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
     static constexpr int B_PVDONE = B_SFREE + 2;    // 2: a P.V product of tile t completed
-    static constexpr int B_EFREE = B_PVDONE + 2;    // 2: staging block of tile t free
-    static constexpr int B_EFULL = B_EFREE + 2;     // 2: staging block of tile t written
-    static constexpr int B_DRAIN = B_EFULL + 2;     // 1
+    static constexpr int B_DRAIN = B_PVDONE + 2;    // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_CTL + 16;
@@ -354,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_o, const Params p) {
+                    const Params p) {
     using C = Cfg<D, F8>;
     static_assert(!F8 || (D == 128 && !DEC), "e4m3 operands: d = 128, plain forward");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -385,8 +379,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(C::B_OFULL + t), 1);
             ptx::mbar_init(bar(C::B_SFREE + t), 4);
             ptx::mbar_init(bar(C::B_PVDONE + t), 1);
-            ptx::mbar_init(bar(C::B_EFREE + t), 1);
-            ptx::mbar_init(bar(C::B_EFULL + t), 4);
         }
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
@@ -396,7 +388,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
-        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == WARP_MMA) {
         ptx::tmem_alloc(sb + C::SMEM_CTL, TMEM_COLS);
@@ -685,11 +676,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
         const uint32_t t_p = tmem + lane_off + (t ? C::COL_P1 : C::COL_P0);
-        uint8_t *stage_ptr = smem + C::SMEM_STAGE + t * C::STAGE_BYTES;
-        const uint32_t stage_addr = sb + C::SMEM_STAGE + t * C::STAGE_BYTES;
-        const bool store_thread = (quad == 0 && lane == 0);  // issues this warpgroup's O stores
-        const uint32_t bar_efree = bar(C::B_EFREE + t), bar_efull = bar(C::B_EFULL + t);
-        uint32_t e_use = 0;
         // decode shape: tile row r holds query r % Nq (of head r / Nq of the group)
         int my_dec_pos = 0;
         if constexpr (DEC) my_dec_pos = p.pos_off + (row - fdiv(row, p.div_nq) * p.Nq);
@@ -891,13 +877,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 ptx::tc_fence_after();
             }
-            // epilogue: O / (sum of rounded P) -> bf16 -> staging block -> TMA store (rows
-            // past the sequence end are clipped by the store), and the natural-log LSE
+            // epilogue: O / (sum of rounded P) and the natural-log LSE
             const float inv_l = r_run > 0.f ? v_max / r_run : 0.f;
             const size_t ridx = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
-            const int zq = ui.zq;
             if constexpr (DEC) {
                 if (p.splits > 1) {
                     // split of the key sequence: this unit's normalised O (fp32) and LSE go
@@ -930,59 +914,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     continue;
                 }
             }
+            // O / (sum of rounded P) -> bf16, from tensor memory straight to global memory:
+            // each thread writes its own row (2d contiguous bytes; rows past N are
+            // skipped). The tensor-memory loads are warp-collective, so every lane takes
+            // them.
+            {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D);
 #pragma unroll 1
-            for (int h = 0; ok && h < D / 64; ++h) {
-                // the staging block is free once the previous store from it has read it
-                if (store_thread) {
-                    ptx::bulk_wait_group_read0();
-                    ptx::mbar_arrive(bar_efree);
-                }
-                ok = wait_warp(bar_efree, e_use & 1u, abort_flag, limit);
-                if (!ok) break;
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
                     if (!empty) {
-                        ptx::tmem_ld32(t_o + 64 * h + 32 * c2, r);
+                        ptx::tmem_ld32(t_o + 32 * c, r);
                         ptx::tmem_wait_ld();
                     } else {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = 0u;
                     }
+                    if (qi < p.N) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint4 val;
-                        val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 0]) * inv_l,
-                                                 __uint_as_float(r[8 * g + 1]) * inv_l);
-                        val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 2]) * inv_l,
-                                                 __uint_as_float(r[8 * g + 3]) * inv_l);
-                        val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 4]) * inv_l,
-                                                 __uint_as_float(r[8 * g + 5]) * inv_l);
-                        val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 6]) * inv_l,
-                                                 __uint_as_float(r[8 * g + 7]) * inv_l);
-                        // 128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r % 8)
-                        const int chunk = (c2 * 4 + g) ^ (row & 7);
-                        *reinterpret_cast<uint4 *>(stage_ptr + row * 128 + chunk * 16) = val;
+                        for (int g = 0; g < 4; ++g) {
+                            uint4 val;
+                            val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 0]) * inv_l,
+                                                     __uint_as_float(r[8 * g + 1]) * inv_l);
+                            val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 2]) * inv_l,
+                                                     __uint_as_float(r[8 * g + 3]) * inv_l);
+                            val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 4]) * inv_l,
+                                                     __uint_as_float(r[8 * g + 5]) * inv_l);
+                            val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g + 6]) * inv_l,
+                                                     __uint_as_float(r[8 * g + 7]) * inv_l);
+                            dst[4 * c + g] = val;
+                        }
                     }
                 }
-                ptx::fence_proxy_async_shared();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_efull);
-                if (quad == 0) {
-                    ok = wait_warp(bar_efull, e_use & 1u, abort_flag, limit);
-                    if (ok && store_thread) {
-                        ptx::tma_store_3d(&tm_o, stage_addr, 64 * h, q0, zq);
-                        ptx::bulk_commit_group();
-                    }
-                }
-                ++e_use;
             }
             if (!ok) break;
             if (qi < p.N) p.lse[ridx] = lse_nat;
         }
-        // the O stores read shared memory and write global memory after they are issued:
-        // both must be done before the CTA exits
-        if (store_thread) ptx::bulk_wait_group0();
     }
 
     ptx::tc_fence_before();
@@ -1379,12 +1346,11 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, con
            int sms) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     int rc;
     if ((rc = encode_map(enc, &mq, q, D, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mk, k, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
-    if ((rc = encode_map(enc, &mo, o, D, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     attn::Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
@@ -1416,7 +1382,7 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, con
     p.o_part = p.lse_part = nullptr;
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, false, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    attn::attn_fwd_kernel<D, false, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
@@ -1428,12 +1394,11 @@ int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, 
                float scale, cudaStream_t stream, int sms) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cuda_fail(cudaErrorNotSupported);
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     int rc;
     if ((rc = encode_map_u8(enc, &mq, q8, 128, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     if ((rc = encode_map_u8(enc, &mk, k8, 128, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
     if ((rc = encode_map_u8(enc, &mv, v8, 128, N, static_cast<long long>(B) * Hkv)) != ATTN_OK) return rc;
-    if ((rc = encode_map(enc, &mo, o, 128, N, static_cast<long long>(B) * Hq)) != ATTN_OK) return rc;
     attn::Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
@@ -1467,7 +1432,7 @@ int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, 
     p.v_scale = vs;
     const int grid = p.num_units < sms ? p.num_units : sms;
     attn::attn_fwd_kernel<128, false, true><<<grid, attn::NUM_THREADS, Cfg<128, true>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, mo, p);
+        mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
@@ -1551,12 +1516,11 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
         if (misaligned(workspace, 256)) return ATTN_ERR_ALIGN;
         if (workspace_bytes < decode_workspace(rows, D, splits)) return ATTN_ERR_WORKSPACE;
     }
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     int rc;
     if ((rc = encode_map(enc, &mq, q, D, R, bhkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mk, k, D, Nk, bhkv)) != ATTN_OK) return rc;
     if ((rc = encode_map(enc, &mv, v, D, Nk, bhkv)) != ATTN_OK) return rc;
-    if ((rc = encode_map(enc, &mo, o, D, R, bhkv)) != ATTN_OK) return rc;
     attn::Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
@@ -1596,7 +1560,7 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
         p.o_part = p.lse_part = nullptr;
     }
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, mo, p);
+    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     if (splits > 1) {
