@@ -16,11 +16,18 @@ Parity status of each function (see the pins in ``tests/test_oracle_pins.py`` an
   form, brute force and torch SDPA with an offset mask).
   attn_ref_bwd -- pinned (torch autograd through fp64 scaled_dot_product_attention with
   the same masks, central finite differences of the oracle's own forward, and the
-  invariants sum_j ds_ij = 0 and dv = sum of p^T do).
+  invariants sum_j ds_ij = 0 and dv = sum of p^T do). Its given-o form is pinned by
+  equality with the chain-rule form for the exact o and by the closed-form response to
+  a change of one element of o; attn_ref_bwd_dq_rows by equality with its dq on every
+  row.
   e4m3_encode / e4m3_decode / quantize_e4m3_blocks / attn_ref_fp8 -- pinned (every code
   against torch's float8_e4m3fn, the rounding of every bf16 value in range, block
   reconstruction bounds, exactness on representable inputs, and the block-vs-tensor
   scaling error comparison the FlashAttention-3 review reports).
+  hadamard / incoherent / quantize_e4m3_blocks_f64 / attn_ref_fp8(signs=...) -- pinned
+  (the Sylvester matrix against scipy's and H H^T = d I, one-hot rows, preserved scores
+  and attention, quantiser bounds and agreement with the fp32 quantiser where both scale
+  by exactly 1, and lower error with outlier channels).
 """
 from __future__ import annotations
 
