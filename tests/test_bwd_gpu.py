@@ -244,3 +244,19 @@ def test_bwd_full_size_sampled_dq_rows(name):
     bound = ROW_REL * r + w.scale * delta * knorm + ROW_FLOOR * rms + 1e-6
     bad = np.nonzero(e > bound)[0]
     assert bad.size == 0, f"{name}: {bad.size} dq rows off, first {rows[bad[:5]]}: err {e[bad[:5]]} ref {r[bad[:5]]}"
+
+
+def test_bwd_is_deterministic_and_stream_ordered():
+    # no atomics: two runs give identical bits, also on a side stream
+    q, k, v = make_qkv(2, 8, 2, 700, 128, 5900)
+    do = make_dout(2, 8, 700, 128, 5901)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = ea.attn_fwd(qd, kd, vd, causal=True)
+    a = ea.attn_bwd(qd, kd, vd, out, lse, dod, causal=True)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b = ea.attn_bwd(qd, kd, vd, out, lse, dod, causal=True, stream=side)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
