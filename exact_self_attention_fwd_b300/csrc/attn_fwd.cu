@@ -749,11 +749,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const bool none = c_hi < c_lo || !row_live;
                     const uint32_t span = none ? 0u : static_cast<uint32_t>(c_hi - c_lo);
                     const uint32_t base = none ? 0xFFFFFFFFu : static_cast<uint32_t>(c_lo);
+                    // The warp's 32 rows decide each 32-column chunk together: a chunk that
+                    // lies inside every row's interval is skipped, and only the others are
+                    // compared element by element (on a diagonal tile, warp w skips the w
+                    // chunks left of the diagonal; at a ragged sequence end, the chunks
+                    // before it). An empty row counts as the interval [BN, -1]. (A third,
+                    // all -inf branch for chunks outside every interval made the compiler
+                    // spill the S registers.)
+                    const int lo_r = none ? BN : c_lo, hi_r = none ? -1 : c_hi;
+                    const int lo_max = __reduce_max_sync(0xffffffffu, lo_r);
+                    const int hi_min = __reduce_min_sync(0xffffffffu, hi_r);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
+                        if (!(lo_max <= 32 * c && hi_min >= 32 * c + 31)) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            sr[c][e] = ptx::mask_above(sr[c][e], static_cast<uint32_t>(c * 32 + e) - base, span);
+                            for (int e = 0; e < 32; ++e)
+                                sr[c][e] = ptx::mask_above(sr[c][e], static_cast<uint32_t>(c * 32 + e) - base, span);
+                        }
                     }
                 }
                 // row maximum: four independent chains of three-input max
