@@ -1052,6 +1052,11 @@ __global__ void __launch_bounds__(256, 2) quantize_hadamard_e4m3_kernel(const __
     const int part = lane & 7;  // which 16 channels of the row
     // channels 16 part .. 16 part + 15 whose sign is flipped (bit c of the 128-bit mask)
     const uint32_t neg = static_cast<uint32_t>((part < 4 ? neg_lo : neg_hi) >> (16 * (part & 3))) & 0xFFFFu;
+    // the flips as XOR masks on the sign bits of the packed bf16 pairs (an exact negation)
+    uint32_t flip[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        flip[i] = (((neg >> (2 * i)) & 1u) << 15) | (((neg >> (2 * i + 1)) & 1u) << 31);
     float y[PASSES][16];
     float amax = 0.f;
 #pragma unroll
@@ -1064,16 +1069,14 @@ __global__ void __launch_bounds__(256, 2) quantize_hadamard_e4m3_kernel(const __
             const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                v[2 * i] = __uint_as_float(w[i] << 16);
-                v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                const uint32_t ws = w[i] ^ flip[i];
+                v[2 * i] = __uint_as_float(ws << 16);
+                v[2 * i + 1] = __uint_as_float(ws & 0xFFFF0000u);
             }
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if ((neg >> i) & 1u) v[i] = -v[i];
         // index bits 0-3 inside the lane: pairs (i, i + 2^b) for i with bit b clear
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -1086,14 +1089,15 @@ __global__ void __launch_bounds__(256, 2) quantize_hadamard_e4m3_kernel(const __
             }
         }
         // index bits 4-6 = lane bits 0-2: the lane with the bit clear keeps x_i + x_j,
-        // its partner x_i - x_j
+        // its partner x_i - x_j, both as one fma with a factor of +-1 (the same single
+        // rounding as the sum or difference)
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
-            const bool upper = (lane >> k) & 1;
+            const float sg = ((lane >> k) & 1) ? -1.f : 1.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float pv = __shfl_xor_sync(0xffffffffu, v[i], 1 << k);
-                v[i] = upper ? pv - v[i] : v[i] + pv;
+                v[i] = fmaf(v[i], sg, pv);
             }
         }
 #pragma unroll
