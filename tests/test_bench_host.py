@@ -128,3 +128,26 @@ def test_decode_accounting():
     wb = DecodeWorkload("t", 2, 8, 2, 3, 10, 64, False, 0)
     assert bench.decode_flops(wb) == 4 * 2 * 8 * 30 * 64
     assert bench.decode_hbm_bytes(w) == 2 * (2 * 8 * 3 * 64 * 2) + 2 * (2 * 2 * 10 * 64 * 2) + 2 * 8 * 3 * 4
+
+
+def test_kernel_sha_covers_the_forward_kernel_only(tmp_path, monkeypatch):
+    # the hash follows the forward kernel's device code, its launch function and ptx.cuh,
+    # and ignores the rest of the translation unit (quantisers, decode merge, backward)
+    for rel in bench.KERNEL_SOURCES:
+        dst = tmp_path / rel
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        dst.write_bytes(open(os.path.join(ROOT, rel), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_sha()
+    assert base == bench.kernel_sha() and len(base) == 16
+    cu = next(tmp_path / rel for rel in bench.KERNEL_SOURCES if rel.endswith("attn_fwd.cu"))
+    src = cu.read_text()
+    assert src.count("// Block quantisation to e4m3") == 1 and src.count("int launch(const void *q") == 1
+    # an edit to a later kernel (the e4m3 quantiser) leaves the hash alone
+    cu.write_text(src.replace("// Block quantisation to e4m3", "// Block quantisation to e4m3\n// x", 1))
+    assert bench.kernel_sha() == base
+    # an edit inside the forward kernel changes it
+    cu.write_text(src.replace("attn_fwd_kernel(", "attn_fwd_kernel (", 1))
+    assert bench.kernel_sha() != base
+    cu.write_text(src)
+    assert bench.kernel_sha() == base
