@@ -237,3 +237,28 @@ def test_padding_many_units():
     key_len = [int(x) for x in rng.integers(0, 1025, size=24)]
     check_masked(24, 8, 2, 1024, 128, True, 0, seed=4400, key_len=key_len)
     check_masked(24, 8, 8, 1024, 64, False, 0, seed=4401, key_len=key_len)
+
+
+# ------------------------------------------------------------ mask edges on 32-column chunks
+# Edge tiles skip, warp by warp, the 32-column chunks inside every row's key interval and
+# compare the rest element by element. These place the sequence end, the window's lower
+# edge and the padding length exactly on chunk boundaries and one past them.
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [32, 33, 64, 96, 160, 192, 224, 225])
+def test_sequence_end_on_chunk_boundaries(N, d, causal):
+    check_full(1, 2, 1, N, d, causal, 0, seed=5000 + N + d + int(causal))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("W", [32, 33, 96, 160, 224])
+def test_window_edge_on_chunk_boundaries(W, d):
+    check_full(1, 2, 1, 450, d, True, W, seed=5100 + W + d)
+    check_masked(1, 2, 1, 450, d, False, W, seed=5200 + W + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_padding_on_chunk_boundaries(d):
+    key_len = [32, 64, 96, 160, 192, 224, 31, 97]
+    check_masked(len(key_len), 2, 1, 256, d, True, 0, seed=5300 + d, key_len=key_len)
+    check_masked(len(key_len), 2, 1, 256, d, False, 0, seed=5400 + d, key_len=key_len)
