@@ -87,7 +87,8 @@ def _declare(lib):
                                                   ctypes.POINTER(ctypes.c_float)]
     lib.attn_ref_quantize_e4m3_blocks.restype = ctypes.c_int
     lib.attn_ref_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
-                                     ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p]
+                                     ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p, f64p,
+                                     ctypes.c_int]
     lib.attn_ref_bwd_f64.restype = ctypes.c_int
     lib.attn_ref_bwd_dq_rows_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                              ctypes.c_double, ctypes.POINTER(ctypes.c_int32),
@@ -98,7 +99,7 @@ def _declare(lib):
     lib.attn_ref_quantize_e4m3_blocks_f64.restype = ctypes.c_int
     lib.attn_ref_bwd_given_o_f64.argtypes = [u16p, u16p, u16p, u16p, f64p, i64, i64, i64, i64, i64, ctypes.c_int,
                                              i64, ctypes.c_double, ctypes.POINTER(ctypes.c_int32), f64p, f64p,
-                                             f64p]
+                                             f64p, ctypes.c_int]
     lib.attn_ref_bwd_given_o_f64.restype = ctypes.c_int
     return lib
 
@@ -381,9 +382,12 @@ def attn_ref_fp8(q, k, v, causal: bool = False, window: int = 0, scale: float | 
 
 
 def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: float | None = None,
-                 key_len=None, lib=None, o=None):
+                 key_len=None, lib=None, o=None, nthreads: int | None = None):
     """fp64 gradients (dq [B,Hq,N,d], dk, dv [B,Hkv,N,d]) of the forward's o for the
     upstream gradient do [B,Hq,N,d] (all inputs bf16).
+
+    nthreads: threads over slices of query rows (default: every core this process may
+    use); the dk, dv partials of the slices are added in slice order.
 
     o: None, or a given forward output [B,Hq,N,d] (any float type, taken as fp64): the
     softmax row sum of dp is then formed as do_i . o_i from it, as a backward pass that
@@ -407,7 +411,8 @@ def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: floa
             qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
             ob.ctypes.data_as(f64p), B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
             kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
-            dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p))
+            dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p),
+            int(nthreads or default_threads()))
         if rc != 0:
             raise ValueError(f"oracle rejected the arguments (code {rc})")
         return dq, dk, dv
@@ -415,7 +420,8 @@ def attn_ref_bwd(q, k, v, do, causal: bool = False, window: int = 0, scale: floa
         qb.ctypes.data_as(u16p), kb.ctypes.data_as(u16p), vb.ctypes.data_as(u16p), db.ctypes.data_as(u16p),
         B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
         kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
-        dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p))
+        dq.ctypes.data_as(f64p), dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p),
+        int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return dq, dk, dv

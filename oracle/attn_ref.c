@@ -400,7 +400,14 @@ int attn_ref_quantize_e4m3_blocks_f64(const double *x, int64_t BH, int64_t N, in
  *   dv_j  = sum over (query head of the group, i) of p_ij do_i
  *
  * Inputs bf16 bits (q, k, v, do_ as for the forward); outputs fp64, dq [B,Hq,N,d], dk and
- * dv [B,Hkv,N,d]. Single-threaded over heads (test sizes only).
+ * dv [B,Hkv,N,d].
+ *
+ * Threads: the flat query rows (b * Hq + hq) * N + i are split into contiguous slices,
+ * one per thread. dq rows are disjoint between slices. Each slice adds its dk and dv
+ * terms into private buffers that cover the key-value heads its rows read, and the
+ * buffers are then added into dk and dv in slice order, so a given thread count always
+ * gives the same bits. With one thread the sums are formed in exactly the order of a
+ * plain loop over b, hq, i.
  *
  * o_in: NULL, or a given forward output [B,Hq,N,d] (fp64). A backward pass that takes
  * the forward's output as an input forms the row sum sum_l p_il dp_il as do_i . o_i,
@@ -408,93 +415,163 @@ int attn_ref_quantize_e4m3_blocks_f64(const double *x, int64_t BH, int64_t N, in
  * given o_in the row sum is do_i . o_in_i, so the gradients are those a backward pass
  * computes from that o.
  */
-static int bwd_core(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
-                    const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
-                    int causal, int64_t window, double scale, const int32_t *key_len,
-                    double *dq, double *dk, double *dv) {
-    if (!q || !k || !v || !do_ || !dq || !dk || !dv) return -1;
-    int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
-    if (rc) return rc;
-    const int64_t group = Hq / Hkv;
+typedef struct {
+    const uint16_t *q, *k, *v, *do_;
+    const double *o_in;
+    int64_t B, Hq, Hkv, N, d, window, group;
+    int causal;
+    double scale;
+    const int32_t *key_len;
+    int64_t row_begin, row_end; /* flat query rows of this slice */
+    int64_t kv_first;           /* first flat key-value head (b * Hkv + kv) the slice reads */
+    double *dq;                 /* shared; the slice writes only its own rows */
+    double *dk, *dv;            /* private, from head kv_first on */
+    int rc;
+} bwd_job_t;
+
+static void *bwd_worker(void *arg) {
+    bwd_job_t *jb = (bwd_job_t *)arg;
+    const int64_t N = jb->N, d = jb->d, Hq = jb->Hq, Hkv = jb->Hkv;
     double *p = (double *)malloc(sizeof(double) * (size_t)N);
     double *dp = (double *)malloc(sizeof(double) * (size_t)N);
     if (!p || !dp) {
         free(p);
         free(dp);
-        return -5;
+        jb->rc = -5;
+        return NULL;
     }
-    for (int64_t i = 0; i < B * Hq * N * d; ++i) dq[i] = 0.0;
-    for (int64_t i = 0; i < B * Hkv * N * d; ++i) dk[i] = dv[i] = 0.0;
-    for (int64_t b = 0; b < B; ++b) {
-        int64_t L = key_len ? (int64_t)key_len[b] : N;
+    for (int64_t r = jb->row_begin; r < jb->row_end; ++r) {
+        const int64_t bh = r / N, i = r % N, b = bh / Hq, hq = bh % Hq, kv = hq / jb->group;
+        int64_t L = jb->key_len ? (int64_t)jb->key_len[b] : N;
         if (L < 0) L = 0;
         if (L > N) L = N;
-        for (int64_t hq = 0; hq < Hq; ++hq) {
-            const int64_t kv = hq / group;
-            const uint16_t *qh = q + (b * Hq + hq) * N * d, *doh = do_ + (b * Hq + hq) * N * d;
-            const uint16_t *kh = k + (b * Hkv + kv) * N * d, *vh = v + (b * Hkv + kv) * N * d;
-            double *dqh = dq + (b * Hq + hq) * N * d;
-            double *dkh = dk + (b * Hkv + kv) * N * d, *dvh = dv + (b * Hkv + kv) * N * d;
-            for (int64_t i = 0; i < N; ++i) {
-                /* scores, their maximum and the log-sum-exp over the visible keys */
-                double m = -INFINITY;
-                int64_t nvis = 0;
-                for (int64_t j = 0; j < N; ++j) {
-                    p[j] = 0.0;
-                    if (!key_visible(i, j, causal, window, L)) continue;
-                    double dot = 0.0;
-                    for (int64_t c = 0; c < d; ++c)
-                        dot += bf16_bits_to_double(qh[i * d + c]) * bf16_bits_to_double(kh[j * d + c]);
-                    p[j] = scale * dot; /* the score, for now */
-                    if (p[j] > m) m = p[j];
-                    ++nvis;
-                }
-                if (nvis == 0) continue; /* a row with no visible key contributes nothing */
-                double l = 0.0;
-                for (int64_t j = 0; j < N; ++j)
-                    if (key_visible(i, j, causal, window, L)) l += exp(p[j] - m);
-                const double lse = m + log(l);
-                double pdp = 0.0;
-                for (int64_t j = 0; j < N; ++j) {
-                    if (!key_visible(i, j, causal, window, L)) {
-                        p[j] = 0.0;
-                        dp[j] = 0.0;
-                        continue;
-                    }
-                    p[j] = exp(p[j] - lse);
-                    double dot = 0.0;
-                    for (int64_t c = 0; c < d; ++c)
-                        dot += bf16_bits_to_double(doh[i * d + c]) * bf16_bits_to_double(vh[j * d + c]);
-                    dp[j] = dot;
-                    pdp += p[j] * dp[j];
-                }
-                if (o_in) {
-                    const double *oi = o_in + ((b * Hq + hq) * N + i) * d;
-                    pdp = 0.0;
-                    for (int64_t c = 0; c < d; ++c) pdp += bf16_bits_to_double(doh[i * d + c]) * oi[c];
-                }
-                for (int64_t j = 0; j < N; ++j) {
-                    if (p[j] == 0.0 && dp[j] == 0.0) continue;
-                    const double ds = p[j] * (dp[j] - pdp);
-                    for (int64_t c = 0; c < d; ++c) {
-                        dqh[i * d + c] += scale * ds * bf16_bits_to_double(kh[j * d + c]);
-                        dkh[j * d + c] += scale * ds * bf16_bits_to_double(qh[i * d + c]);
-                        dvh[j * d + c] += p[j] * bf16_bits_to_double(doh[i * d + c]);
-                    }
-                }
+        const uint16_t *qh = jb->q + bh * N * d, *doh = jb->do_ + bh * N * d;
+        const uint16_t *kh = jb->k + (b * Hkv + kv) * N * d, *vh = jb->v + (b * Hkv + kv) * N * d;
+        double *dqh = jb->dq + bh * N * d;
+        double *dkh = jb->dk + (b * Hkv + kv - jb->kv_first) * N * d;
+        double *dvh = jb->dv + (b * Hkv + kv - jb->kv_first) * N * d;
+        /* scores, their maximum and the log-sum-exp over the visible keys */
+        double m = -INFINITY;
+        int64_t nvis = 0;
+        for (int64_t j = 0; j < N; ++j) {
+            p[j] = 0.0;
+            if (!key_visible(i, j, jb->causal, jb->window, L)) continue;
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += bf16_bits_to_double(qh[i * d + c]) * bf16_bits_to_double(kh[j * d + c]);
+            p[j] = jb->scale * dot; /* the score, for now */
+            if (p[j] > m) m = p[j];
+            ++nvis;
+        }
+        if (nvis == 0) continue; /* a row with no visible key contributes nothing */
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            if (key_visible(i, j, jb->causal, jb->window, L)) l += exp(p[j] - m);
+        const double lse = m + log(l);
+        double pdp = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (!key_visible(i, j, jb->causal, jb->window, L)) {
+                p[j] = 0.0;
+                dp[j] = 0.0;
+                continue;
+            }
+            p[j] = exp(p[j] - lse);
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += bf16_bits_to_double(doh[i * d + c]) * bf16_bits_to_double(vh[j * d + c]);
+            dp[j] = dot;
+            pdp += p[j] * dp[j];
+        }
+        if (jb->o_in) {
+            const double *oi = jb->o_in + (bh * N + i) * d;
+            pdp = 0.0;
+            for (int64_t c = 0; c < d; ++c) pdp += bf16_bits_to_double(doh[i * d + c]) * oi[c];
+        }
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0 && dp[j] == 0.0) continue;
+            const double ds = p[j] * (dp[j] - pdp);
+            for (int64_t c = 0; c < d; ++c) {
+                dqh[i * d + c] += jb->scale * ds * bf16_bits_to_double(kh[j * d + c]);
+                dkh[j * d + c] += jb->scale * ds * bf16_bits_to_double(qh[i * d + c]);
+                dvh[j * d + c] += p[j] * bf16_bits_to_double(doh[i * d + c]);
             }
         }
     }
     free(p);
     free(dp);
-    return 0;
+    return NULL;
+}
+
+static int bwd_core(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                    const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
+                    int causal, int64_t window, double scale, const int32_t *key_len,
+                    double *dq, double *dk, double *dv, int nthreads) {
+    if (!q || !k || !v || !do_ || !dq || !dk || !dv) return -1;
+    int rc = check_args(B, Hq, Hkv, N, d, causal, window, scale);
+    if (rc) return rc;
+    const int64_t group = Hq / Hkv, nrows = B * Hq * N;
+    for (int64_t i = 0; i < B * Hq * N * d; ++i) dq[i] = 0.0;
+    for (int64_t i = 0; i < B * Hkv * N * d; ++i) dk[i] = dv[i] = 0.0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nrows) nthreads = (int)nrows;
+    bwd_job_t *jobs = (bwd_job_t *)calloc((size_t)nthreads, sizeof(bwd_job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int ok = jobs && tids;
+    for (int t = 0; ok && t < nthreads; ++t) {
+        bwd_job_t *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->do_ = do_; jb->o_in = o_in;
+        jb->B = B; jb->Hq = Hq; jb->Hkv = Hkv; jb->N = N; jb->d = d;
+        jb->window = window; jb->group = group; jb->causal = causal; jb->scale = scale;
+        jb->key_len = key_len;
+        jb->row_begin = nrows * t / nthreads;
+        jb->row_end = nrows * (t + 1) / nthreads;
+        jb->dq = dq;
+        /* rows of head bh read key-value head bh / group (b * Hkv + hq / group) */
+        jb->kv_first = (jb->row_begin / N) / group;
+        const int64_t kv_last = ((jb->row_end - 1) / N) / group;
+        const size_t n = (size_t)(kv_last - jb->kv_first + 1) * (size_t)(N * d);
+        jb->dk = (double *)calloc(n, sizeof(double));
+        jb->dv = (double *)calloc(n, sizeof(double));
+        if (!jb->dk || !jb->dv) ok = 0;
+    }
+    if (ok) {
+        int spawned = 0;
+        for (int t = 1; t < nthreads; ++t) {
+            if (pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) != 0) break;
+            spawned = t;
+        }
+        bwd_worker(&jobs[0]);
+        for (int t = 1; t <= spawned; ++t) pthread_join(tids[t], NULL);
+        /* slices whose thread failed to start run here, serially */
+        for (int t = spawned + 1; t < nthreads; ++t) bwd_worker(&jobs[t]);
+        /* the private dk, dv partials, added in slice order */
+        for (int t = 0; t < nthreads; ++t) {
+            const bwd_job_t *jb = &jobs[t];
+            if (jb->rc) ok = 0;
+            const int64_t kv_last = ((jb->row_end - 1) / N) / group;
+            const int64_t off = jb->kv_first * N * d, n = (kv_last - jb->kv_first + 1) * N * d;
+            for (int64_t e = 0; e < n; ++e) {
+                dk[off + e] += jb->dk[e];
+                dv[off + e] += jb->dv[e];
+            }
+        }
+    }
+    if (jobs)
+        for (int t = 0; t < nthreads; ++t) {
+            free(jobs[t].dk);
+            free(jobs[t].dv);
+        }
+    free(jobs);
+    free(tids);
+    return ok ? 0 : -5;
 }
 
 int attn_ref_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
                      int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int causal,
                      int64_t window, double scale, const int32_t *key_len,
-                     double *dq, double *dk, double *dv) {
-    return bwd_core(q, k, v, do_, NULL, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv);
+                     double *dq, double *dk, double *dv, int nthreads) {
+    return bwd_core(q, k, v, do_, NULL, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv,
+                    nthreads);
 }
 
 /*
@@ -575,7 +652,8 @@ int attn_ref_bwd_dq_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_
 int attn_ref_bwd_given_o_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
                              const double *o_in, int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d,
                              int causal, int64_t window, double scale, const int32_t *key_len,
-                             double *dq, double *dk, double *dv) {
+                             double *dq, double *dk, double *dv, int nthreads) {
     if (!o_in) return -1;
-    return bwd_core(q, k, v, do_, o_in, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv);
+    return bwd_core(q, k, v, do_, o_in, B, Hq, Hkv, N, d, causal, window, scale, key_len, dq, dk, dv,
+                    nthreads);
 }

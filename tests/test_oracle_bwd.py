@@ -170,8 +170,8 @@ GIVEN_O_MUTANTS = {
     "given_o_ignored": ("for (int64_t c = 0; c < d; ++c) pdp += bf16_bits_to_double(doh[i * d + c]) * oi[c];",
                         "for (int64_t c = 0; c < d; ++c) pdp += p[0] * 0.0 * oi[c];"),
     # a given output read from the wrong row
-    "given_o_wrong_row": ("const double *oi = o_in + ((b * Hq + hq) * N + i) * d;",
-                          "const double *oi = o_in + ((b * Hq + hq) * N + i / 2) * d;"),
+    "given_o_wrong_row": ("const double *oi = jb->o_in + (bh * N + i) * d;",
+                          "const double *oi = jb->o_in + (bh * N + i / 2) * d;"),
 }
 
 
@@ -192,14 +192,14 @@ BWD_MUTANTS = {
     # the softmax gradient without its row term
     "ds_without_row_term": ("const double ds = p[j] * (dp[j] - pdp);", "const double ds = p[j] * dp[j];"),
     # the key gradient without the score scale
-    "dk_without_scale": ("dkh[j * d + c] += scale * ds * bf16_bits_to_double(qh[i * d + c]);",
+    "dk_without_scale": ("dkh[j * d + c] += jb->scale * ds * bf16_bits_to_double(qh[i * d + c]);",
                          "dkh[j * d + c] += ds * bf16_bits_to_double(qh[i * d + c]);"),
     # the value gradient weighted by the score gradient instead of the probability
     "dv_from_ds": ("dvh[j * d + c] += p[j] * bf16_bits_to_double(doh[i * d + c]);",
                    "dvh[j * d + c] += ds * bf16_bits_to_double(doh[i * d + c]);"),
     # the query gradient from value rows instead of key rows
-    "dq_from_v": ("dqh[i * d + c] += scale * ds * bf16_bits_to_double(kh[j * d + c]);",
-                  "dqh[i * d + c] += scale * ds * bf16_bits_to_double(vh[j * d + c]);"),
+    "dq_from_v": ("dqh[i * d + c] += jb->scale * ds * bf16_bits_to_double(kh[j * d + c]);",
+                  "dqh[i * d + c] += jb->scale * ds * bf16_bits_to_double(vh[j * d + c]);"),
 }
 
 
@@ -245,3 +245,21 @@ def test_dq_rows_match_full_backward():
         np.testing.assert_allclose(dq_rows, dq.reshape(-1, d), atol=1e-12, rtol=0)
     with pytest.raises(ValueError):
         oracle.attn_ref_bwd_dq_rows(q, k, v, do, [B * Hq * N], causal=True, scale=0.3)
+
+
+def test_bwd_thread_count_changes_only_rounding():
+    # the threads split the query rows into slices whose dk, dv partials are added in
+    # slice order: any thread count gives the one-thread gradients up to fp64 rounding,
+    # and the same count gives the same bits. Slices here split heads and groups.
+    g = torch.Generator().manual_seed(61)
+    B, Hq, Hkv, N, d = 2, 4, 2, 41, 16
+    q = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    k, v = (torch.randn(B, Hkv, N, d, generator=g).bfloat16() for _ in range(2))
+    do = torch.randn(B, Hq, N, d, generator=g).bfloat16()
+    one = oracle.attn_ref_bwd(q, k, v, do, causal=True, window=9, scale=0.3, nthreads=1)
+    for n in (2, 7, 13, B * Hq * N + 5):
+        many = oracle.attn_ref_bwd(q, k, v, do, causal=True, window=9, scale=0.3, nthreads=n)
+        again = oracle.attn_ref_bwd(q, k, v, do, causal=True, window=9, scale=0.3, nthreads=n)
+        for a, b, c in zip(one, many, again):
+            np.testing.assert_allclose(b, a, atol=1e-12, rtol=0)
+            assert np.array_equal(b, c)
