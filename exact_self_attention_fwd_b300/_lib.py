@@ -48,6 +48,8 @@ def _declare(lib):
     lib.attn_fwd.restype = i
     lib.attn_fwd_padded.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     lib.attn_fwd_padded.restype = i
+    lib.attn_fwd_o32.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.attn_fwd_o32.restype = i
     lib.attn_fwd_decode_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.attn_fwd_decode_workspace_size.restype = ctypes.c_size_t
     lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
@@ -131,10 +133,12 @@ def _check_tensors(q, k, v):
 
 
 def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None = None,
-             out=None, lse=None, stream=None, key_len=None):
+             out=None, lse=None, stream=None, key_len=None, out_fp32: bool = False):
     """O [B,Hq,N,d] bf16 and LSE [B,Hq,N] fp32 for CUDA bf16 q [B,Hq,N,d], k/v [B,Hkv,N,d].
 
     key_len: optional CUDA int32 [B] of valid lengths (right padding; attn_fwd_padded).
+    out_fp32: write O as fp32 instead (attn_fwd_o32: the same kernel, O not rounded to
+    bf16), to see the kernel's error apart from the output format.
     Asynchronous on `stream` (default: the current stream of q's device).
     """
     import torch
@@ -144,12 +148,13 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
         raise ValueError("q, k, v must be CUDA tensors on one device")
     if scale is None:
         scale = d ** -0.5
+    o_dtype = torch.float32 if out_fp32 else torch.bfloat16
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=o_dtype, device=dev)
     if lse is None:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != dev:
-        raise ValueError("out must be a contiguous bf16 CUDA tensor shaped like q")
+    if out.shape != q.shape or out.dtype != o_dtype or not out.is_contiguous() or out.device != dev:
+        raise ValueError(f"out must be a contiguous {o_dtype} CUDA tensor shaped like q")
     if tuple(lse.shape) != (B, Hq, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != dev:
         raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, Hq, N]")
     L = load()
@@ -158,7 +163,11 @@ def attn_fwd(q, k, v, causal: bool = False, window: int = 0, scale: float | None
                 or not key_len.is_contiguous()):
             raise ValueError("key_len must be a contiguous int32 CUDA tensor with B entries")
     with torch.cuda.device(dev):
-        if key_len is None:
+        if out_fp32:
+            rc = L.attn_fwd_o32(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                None if key_len is None else key_len.data_ptr(), B, Hq, Hkv, N, d,
+                                int(bool(causal)), int(window), float(scale), _stream_handle(stream, dev))
+        elif key_len is None:
             rc = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                             B, Hq, Hkv, N, d, int(bool(causal)), int(window), float(scale),
                             _stream_handle(stream, dev))

@@ -76,6 +76,8 @@ __device__ unsigned int g_status;  // bit 0: some wait ran out of time
 // must not use the name as a device address: the address comes from
 // cudaGetSymbolAddress, taken once per device.
 constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;  // 8 MiB
+static_assert(NOALLOC_SCRATCH_BYTES == ATTN_DECODE_NOALLOC_SCRATCH_BYTES,
+              "the scratch size must match the limit the header states");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 // Division of a non-negative int below 2^31 by an invariant divisor d >= 1, by a
@@ -120,6 +122,7 @@ struct Params {
     int Nq, splits, split_lo, split_len, split_hi;
     FastDiv div_splits, div_nq;
     float *o_part, *lse_part;  // partial results per split (splits > 1), fp32
+    float *o32;                // plain forward: O as fp32 instead of bf16 (null: bf16 to o)
     // e4m3 operands: per-block scales [z index][ceil(N / 128)] of Q, K and V
     const float *q_scale, *k_scale, *v_scale;
 };
@@ -753,8 +756,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // lies inside every row's interval is skipped, and only the others are
                     // compared element by element (on a diagonal tile, warp w skips the w
                     // chunks left of the diagonal; at a ragged sequence end, the chunks
-                    // before it). An empty row counts as the interval [BN, -1]. (A third,
-                    // all -inf branch for chunks outside every interval made the compiler
+                    // before it). An empty row counts as the interval [BN, -1]. The skip
+                    // test needs c_lo >= 0 (the max above): a negative lower end would make
+                    // lo_max understate where some row's interval starts. (A third, all
+                    // -inf branch for chunks outside every interval made the compiler
                     // spill the S registers.)
                     const int lo_r = none ? BN : c_lo, hi_r = none ? -1 : c_hi;
                     const int lo_max = __reduce_max_sync(0xffffffffu, lo_r);
@@ -894,37 +899,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const size_t ridx = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            // fp32 rows: the split results of the decode shape (merged later by the
+            // combine kernel), or the plain forward's O when fp32 output was asked for.
+            // The tensor-memory loads are warp-collective: every lane takes them, and
+            // only rows of the tile store.
+            float *o32_row = nullptr;
+            float *lse32 = p.lse;
+            size_t lse_idx = ridx;
             if constexpr (DEC) {
                 if (p.splits > 1) {
-                    // split of the key sequence: this unit's normalised O (fp32) and LSE go
-                    // to the partial buffers, which the combine kernel merges. The
-                    // tensor-memory loads are warp-collective: every lane takes them, and
-                    // only rows of the packed tile store.
-                    const bool store_row = qi < p.N;
                     const size_t prow = static_cast<size_t>(ui.split) * rows_per_split(p) + ridx;
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D);
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        if (!empty) {
-                            ptx::tmem_ld32(t_o + 32 * c, r);
-                            ptx::tmem_wait_ld();
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) r[e] = 0u;
-                        }
-                        if (store_row) {
-#pragma unroll
-                            for (int g = 0; g < 8; ++g)
-                                dst[c * 8 + g] = make_float4(__uint_as_float(r[4 * g + 0]) * inv_l,
-                                                             __uint_as_float(r[4 * g + 1]) * inv_l,
-                                                             __uint_as_float(r[4 * g + 2]) * inv_l,
-                                                             __uint_as_float(r[4 * g + 3]) * inv_l);
-                        }
-                    }
-                    if (store_row) p.lse_part[prow] = lse_nat;
-                    continue;
+                    o32_row = p.o_part + prow * D;
+                    lse32 = p.lse_part;
+                    lse_idx = prow;
                 }
+            } else {
+                if (p.o32) o32_row = p.o32 + ridx * D;
+            }
+            if (o32_row) {
+                const bool store_row = qi < p.N;
+                float4 *dst = reinterpret_cast<float4 *>(o32_row);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    if (!empty) {
+                        ptx::tmem_ld32(t_o + 32 * c, r);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = 0u;
+                    }
+                    if (store_row) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            dst[c * 8 + g] = make_float4(__uint_as_float(r[4 * g + 0]) * inv_l,
+                                                         __uint_as_float(r[4 * g + 1]) * inv_l,
+                                                         __uint_as_float(r[4 * g + 2]) * inv_l,
+                                                         __uint_as_float(r[4 * g + 3]) * inv_l);
+                    }
+                }
+                if (store_row) lse32[lse_idx] = lse_nat;
+                continue;
             }
             // O / (sum of rounded P) -> bf16, from tensor memory straight to global memory:
             // each thread writes its own row (2d contiguous bytes; rows past N are
@@ -1357,7 +1372,7 @@ int encode_map(EncodeTiledFn enc, CUtensorMap *map, const void *base, int d, int
 }
 
 template <int D>
-int launch(const void *q, const void *k, const void *v, void *o, float *lse, const int *key_len,
+int launch(const void *q, const void *k, const void *v, void *o, float *o32, float *lse, const int *key_len,
            int B, int Hq, int Hkv, int N, int causal, int window, float scale, cudaStream_t stream,
            int sms) {
     EncodeTiledFn enc = get_encoder();
@@ -1396,6 +1411,7 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, con
     p.div_splits = attn::make_fastdiv(1u);
     p.div_nq = attn::make_fastdiv(1u);
     p.o_part = p.lse_part = nullptr;
+    p.o32 = o32;
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     const int grid = p.num_units < sms ? p.num_units : sms;
     attn::attn_fwd_kernel<D, false, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
@@ -1443,6 +1459,7 @@ int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, 
     p.div_splits = attn::make_fastdiv(1u);
     p.div_nq = attn::make_fastdiv(1u);
     p.o_part = p.lse_part = nullptr;
+    p.o32 = nullptr;
     p.q_scale = qs;
     p.k_scale = ks;
     p.v_scale = vs;
@@ -1568,6 +1585,7 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
     p.div_nq = attn::make_fastdiv(static_cast<uint32_t>(Nq));
     p.num_units = static_cast<int>(bhkv * splits);
     p.q_scale = p.k_scale = p.v_scale = nullptr;
+    p.o32 = nullptr;
     if (splits > 1) {
         p.o_part = static_cast<float *>(workspace);
         const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * D * sizeof(float);
@@ -1694,21 +1712,30 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
 
 extern "C" {
 
-static int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
+// o: bf16 output, or (o32 set) the fp32 output; exactly one of the two is written
+static int fwd_common(const void *q, const void *k, const void *v, void *o, float *o32, float *lse,
                       const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
                       int window, float scale, void *stream) {
-    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, window, scale);
+    int rc = validate(q, k, v, o32 ? static_cast<const void *>(o32) : o, lse, B, Hq, Hkv, N, d, causal,
+                      window, scale);
     if (rc != ATTN_OK) return rc;
     int sms = 0;
     if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d == 64) return launch<64>(q, k, v, o, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
-    return launch<128>(q, k, v, o, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
+    if (d == 64) return launch<64>(q, k, v, o, o32, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
+    return launch<128>(q, k, v, o, o32, lse, key_len, B, Hq, Hkv, N, causal, window, scale, s, sms);
 }
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
              int N, int d, int causal, int window, float scale, void *stream) {
-    return fwd_common(q, k, v, o, lse, nullptr, B, Hq, Hkv, N, d, causal, window, scale, stream);
+    return fwd_common(q, k, v, o, nullptr, lse, nullptr, B, Hq, Hkv, N, d, causal, window, scale, stream);
+}
+
+int attn_fwd_o32(const void *q, const void *k, const void *v, float *o32, float *lse, const int *key_len,
+                 int B, int Hq, int Hkv, int N, int d, int causal, int window, float scale, void *stream) {
+    if (!o32) return ATTN_ERR_NULLPTR;
+    if (key_len && misaligned(key_len, 4)) return ATTN_ERR_ALIGN;
+    return fwd_common(q, k, v, nullptr, o32, lse, key_len, B, Hq, Hkv, N, d, causal, window, scale, stream);
 }
 
 int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -1716,7 +1743,7 @@ int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float 
                     float scale, void *stream) {
     if (!key_len) return ATTN_ERR_NULLPTR;
     if (misaligned(key_len, 4)) return ATTN_ERR_ALIGN;
-    return fwd_common(q, k, v, o, lse, key_len, B, Hq, Hkv, N, d, causal, window, scale, stream);
+    return fwd_common(q, k, v, o, nullptr, lse, key_len, B, Hq, Hkv, N, d, causal, window, scale, stream);
 }
 
 size_t attn_fwd_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int splits) {

@@ -110,6 +110,21 @@ int attn_fwd_padded(const void *q, const void *k, const void *v, void *o, float 
                     int window, float scale, void *stream);
 
 /*
+ * attn_fwd_o32 -- attn_fwd (or, with key_len, attn_fwd_padded) writing O as fp32: the
+ * same kernel and arithmetic, with the final O / (sum of rounded P) stored unrounded.
+ * attn_fwd's bf16 O is exactly this value rounded to nearest even. It exists to measure
+ * the kernel's own error apart from the bf16 output format: for |O| in [4, 8) half a
+ * bf16 spacing (2^-6) already exceeds an absolute error bar of 1e-2.
+ *
+ *   o32      device, fp32 [B, Hq, N, d], 16-byte aligned (written)
+ *   key_len  NULL, or as for attn_fwd_padded
+ * Every other argument is as for attn_fwd. ATTN_ERR_NULLPTR when o32 is NULL.
+ */
+int attn_fwd_o32(const void *q, const void *k, const void *v, float *o32, float *lse,
+                 const int *key_len, int B, int Hq, int Hkv, int N, int d, int causal,
+                 int window, float scale, void *stream);
+
+/*
  * attn_fwd_decode -- the decode shape: Nq query rows that are the LAST Nq positions of
  * a sequence of Nk >= Nq tokens whose keys and values are given (a key-value cache read
  * by the newest tokens: the generation stage in the SpAtten review's "Background"
@@ -263,7 +278,9 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
  * before any stream capture. Every call on a device shares the one array and each split
  * overwrites all of its part before the merge reads it, so nothing needs clearing;
  * calls whose kernels overlap on the GPU (different streams, or different host threads)
- * race on it and must be serialised by the caller.
+ * race on it and must be serialised by the caller. The cached address stays valid for
+ * the life of the device's primary context: after cudaDeviceReset on a device, this
+ * entry point must not be called on that device again in the same process.
  */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -246,6 +246,44 @@ def test_bwd_full_size_sampled_dq_rows(name):
     assert bad.size == 0, f"{name}: {bad.size} dq rows off, first {rows[bad[:5]]}: err {e[bad[:5]]} ref {r[bad[:5]]}"
 
 
+@pytest.mark.parametrize("name,b,kv", [("gqa_8k", 1, 5), ("swa_16k", 0, 11)])
+def test_bwd_full_size_one_group_every_element(name, b, kv):
+    """The workload at full size, and every element of dK and dV (and dQ) of one
+    (batch, KV head) group against the oracle's gradients for that group. The group's
+    query heads get the oracle's O rounded to bf16 and its LSE rounded to fp32 (the
+    other heads keep the GPU forward's, which the group's gradients do not read), and
+    the tolerance is the module's: rows within 5u ||ref|| + 2e-3 rms, dV elementwise
+    within 3u of the sum of its terms' magnitudes."""
+    from exact_self_attention_fwd_b300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    do = make_dout(w.B, w.Hq, w.N, w.d, w.seed + 100)
+    G = w.group
+    hs = slice(kv * G, (kv + 1) * G)
+    qg, dog = q[b:b + 1, hs].contiguous(), do[b:b + 1, hs].contiguous()
+    kg, vg = k[b:b + 1, kv:kv + 1].contiguous(), v[b:b + 1, kv:kv + 1].contiguous()
+    o_g, lse_g = oracle.attn_ref(qg, kg, vg, causal=w.causal, window=w.window, scale=w.scale)
+    o_g16 = torch.from_numpy(o_g).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = ea.attn_fwd(qd, kd, vd, causal=w.causal, window=w.window, scale=w.scale)
+    out[b, hs] = o_g16[0].to(DEV)
+    lse[b, hs] = torch.from_numpy(lse_g[0]).float().to(DEV)
+    dq, dk, dv = ea.attn_bwd(qd, kd, vd, out, lse, dod, causal=w.causal, window=w.window, scale=w.scale)
+    torch.cuda.synchronize()
+    assert ea.device_error() == ea.ATTN_OK
+    rq, rk, rv = oracle.attn_ref_bwd(qg, kg, vg, dog, causal=w.causal, window=w.window, scale=w.scale,
+                                     o=o_g16.double())
+    rms = max(rms_rows(rq), rms_rows(rk), rms_rows(rv))
+    label = f"{name} group b{b} kv{kv}"
+    gq, gk, gv = _np(dq[b:b + 1, hs]), _np(dk[b:b + 1, kv:kv + 1]), _np(dv[b:b + 1, kv:kv + 1])
+    res = {n: check_rows(g, r, n, label, rms, np.zeros(r.shape[:-1]))
+           for n, g, r in (("dq", gq, rq), ("dk", gk, rk), ("dv", gv, rv))}
+    _, _, av = oracle.attn_ref_bwd(qg, kg, vg, dog.abs(), causal=w.causal, window=w.window, scale=w.scale)
+    worst = float((np.abs(gv - rv) - (3 * U * av + 1e-6)).max())
+    assert worst <= 0.0, f"{label}: dV exceeds 3u x sum of |terms| by {worst:.3g}"
+    print(label, res)
+
+
 def test_bwd_is_deterministic_and_stream_ordered():
     # no atomics: two runs give identical bits, also on a side stream
     q, k, v = make_qkv(2, 8, 2, 700, 128, 5900)

@@ -54,3 +54,23 @@ def test_format_floor_exception_only_for_large_outputs():
     o[0, 0] = 5.0
     stats = compare(*_as_gpu(o, lse_ref), o_ref, lse_ref, "floor")
     assert stats["o_max_abs"] > 1e-2 and stats["format_floor_exceptions"] == 1
+
+
+def test_strict_bar_has_no_floor_and_no_exceptions():
+    # an fp32 output is held to the plain bar: the element that the bf16 format floor
+    # excuses above fails, and so does a mean error inside the floor allowance
+    o_ref, lse_ref = _case(5)
+    o_ref[0, 0] = 5.015
+    o = o_ref.copy()
+    o[0, 0] = 5.0
+    with pytest.raises(AssertionError, match="strict"):
+        compare(torch.from_numpy(o).float(), torch.from_numpy(lse_ref).float(), o_ref, lse_ref, "strict",
+                strict=True)
+    o_ref, lse_ref = _case(6, n=8)
+    o = o_ref + 1.5e-3
+    with pytest.raises(AssertionError, match="mean"):
+        compare(torch.from_numpy(o).float(), torch.from_numpy(lse_ref).float(), o_ref, lse_ref, "strict mean",
+                strict=True)
+    stats = compare(torch.from_numpy(o_ref).float(), torch.from_numpy(lse_ref).float(), o_ref, lse_ref,
+                    "exact", strict=True)
+    assert stats["o_max_abs"] < 1e-6 and stats["format_floor_exceptions"] == 0

@@ -66,3 +66,44 @@ def test_noalloc_rejects_results_beyond_its_scratch():
     k = torch.zeros(16, 8, 256, 128, dtype=torch.bfloat16, device=DEV)
     rc, _, _ = call_noalloc(q, k, k, True, 0, 0.1, 2)
     assert rc == ea.ATTN_ERR_SCRATCH_LIMIT
+
+
+LIMIT = 8 << 20  # ATTN_DECODE_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_scratch_limit_boundary():
+    # The split results of splits x B x Hq x Nq rows take rows x (4 d + 4) bytes at d = 64
+    # (the 4 d part is already a multiple of the 256-byte alignment): 32263 rows
+    # (7 splits x 419 x 11 heads x 1 query) are the most that fit in 8 MiB, 228 bytes
+    # short of it; 32264 rows (8 x 109 x 37 x 1) are 32 bytes over.
+    fit = (419, 11, 1, 1, 7 * 128, 64, 7)
+    over = (109, 37, 1, 1, 8 * 128, 64, 8)
+    B, Hq, Hkv, Nq, Nk, d, splits = fit
+    assert ea.decode_workspace_size(B, Hq, Hkv, Nq, Nk, d, splits) == 32263 * 260 <= LIMIT
+    q, k, v = make_qkv_decode(B, Hq, Hkv, Nq, Nk, d, 13)
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    rc, o, lse = call_noalloc(q, k, v, True, 0, 0.125, splits)
+    assert rc == ea.ATTN_OK, ea.status_str(rc)
+    o_ref, lse_ref = ea.attn_fwd_decode(q, k, v, causal=True, scale=0.125, splits=splits)
+    torch.cuda.synchronize()
+    assert ea.device_error() == ea.ATTN_OK
+    compare(o, lse, o_ref.double().cpu().numpy(), lse_ref.double().cpu().numpy(), "no-alloc at the limit")
+    B, Hq, Hkv, Nq, Nk, d, splits = over
+    assert ea.decode_workspace_size(B, Hq, Hkv, Nq, Nk, d, splits) == 32264 * 260 > LIMIT
+    q = torch.zeros(B, Hq, Nq, d, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(B, Hkv, Nk, d, dtype=torch.bfloat16, device=DEV)
+    rc, _, _ = call_noalloc(q, k, k, True, 0, 0.125, splits)
+    assert rc == ea.ATTN_ERR_SCRATCH_LIMIT
+
+
+def test_noalloc_rejects_the_librarys_own_split_count_beyond_its_scratch():
+    # splits = 0: one KV head of 128 packed query rows against 1024 key tiles; the
+    # library splits the keys over about one CTA per SM, and the split results of
+    # that count do not fit
+    B, Hq, Hkv, Nq, Nk, d = 1, 128, 1, 1, 1024 * 128, 128
+    need = ea.decode_workspace_size(B, Hq, Hkv, Nq, Nk, d, 0)
+    assert need > LIMIT
+    q = torch.zeros(B, Hq, Nq, d, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(B, Hkv, Nk, d, dtype=torch.bfloat16, device=DEV)
+    rc, _, _ = call_noalloc(q, k, k, True, 0, 0.1, 0)
+    assert rc == ea.ATTN_ERR_SCRATCH_LIMIT
