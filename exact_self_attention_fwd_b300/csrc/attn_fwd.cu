@@ -489,20 +489,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t sf_use0 = 0, sf_use1 = 0;
             bool ok = true;
 
-            // S_t = Q_t K^T: K-major A and B, 16 columns of d per instruction. The
-            // descriptors of later K steps differ only in the start-address field, so
-            // they are formed by adding the byte offset >> 4 to the first one.
+            // S_t = Q_t K^T: K-major A and B, 16 columns of d (32 bytes) per instruction.
+            // The descriptors of later K steps differ only in the start-address field:
+            // four steps of 32 bytes cover one 128-byte swizzled slab, and each slab of
+            // four is issued from one asm statement (one elected lane, one predicate set-up;
+            // the MMA warp's instruction count per MMA bounds how fast it feeds the
+            // tensor core).
             auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
                 const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
                 const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / C::KSTEP; ++kk) {
-                    // each step covers 32 bytes of a 128-byte row; four steps per slab
-                    const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                    if constexpr (F8)
-                        ptx::mma_ss_elect_f8(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
-                    else
-                        ptx::mma_ss_elect(tmem + col_s, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
+                for (int g = 0; g < D / C::KSTEP / 4; ++g) {
+                    const uint64_t off = static_cast<uint64_t>(g * C::CHUNK_BYTES) >> 4;
+                    ptx::mma_ss4_elect<2, F8>(tmem + col_s, qd + off, kd + off, IDESC_S, g > 0 ? 1u : 0u);
                 }
             };
             // O_t (+)= P_t V: P from tensor memory (K-major), V MN-major in shared memory.
@@ -517,18 +516,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int h = 0; h < 2; ++h) {
                     if (!wait_warp(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
                     ptx::tc_fence_after();
+                    // step k16 reads 8 tensor-memory columns of P (KSTEP keys) and the KSTEP
+                    // rows of V after the previous steps' KSTEP * 128 bytes; a bf16 half is
+                    // four steps, issued from one asm statement
+                    if constexpr (!F8) {
+                        const int k0 = h * 4;
+                        ptx::mma_ts4_elect<8, 128>(tmem + col_o, tmem + col_s + k0 * 8, vd + ((k0 * 16 * 128) >> 4),
+                                                   IDESC_PV, (accumulate || h > 0) ? 1u : 0u);
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < BN / C::KSTEP / 2; ++kk) {
-                        // step k16 reads 8 tensor-memory columns of P (KSTEP keys) and the
-                        // KSTEP rows of V after the previous steps' KSTEP * 128 bytes
-                        const int k16 = h * (BN / C::KSTEP / 2) + kk;
-                        const uint64_t vstep = vd + ((k16 * C::KSTEP * 128) >> 4);
-                        if constexpr (F8)
+                        for (int kk = 0; kk < BN / C::KSTEP / 2; ++kk) {
+                            const int k16 = h * (BN / C::KSTEP / 2) + kk;
+                            const uint64_t vstep = vd + ((k16 * C::KSTEP * 128) >> 4);
                             ptx::mma_ts_elect_f8(tmem + col_o, tmem + col_s + k16 * 8, vstep, IDESC_PV,
                                                  (accumulate || k16 > 0) ? 1u : 0u);
-                        else
-                            ptx::mma_ts_elect(tmem + col_o, tmem + col_s + k16 * 8, vstep, IDESC_PV,
-                                              (accumulate || k16 > 0) ? 1u : 0u);
+                        }
                     }
                 }
                 return true;

@@ -186,6 +186,95 @@ __device__ __forceinline__ void mma_ts_elect_f8(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// Four MMAs issued from one asm statement by one elected lane: the k-th MMA uses the
+// descriptors advanced by k x STEP in their start-address field (bits 0-13, in 16-byte
+// units). Shared-memory addresses stay below 2^18 bytes, so the field never carries
+// into bit 14 and a 32-bit add on the low word advances it. The first MMA accumulates
+// when acc0 != 0, the others always accumulate. F8: kind::f8f6f4 (e4m3) instead of
+// kind::f16.
+//   mma_ss4: A and B from shared memory (descriptors), the same STEP for both.
+//   mma_ts4: A from tensor memory (column address advanced by ACOLS per MMA), B from
+//            shared memory advanced by STEP.
+template <uint32_t STEP, bool F8 = false>
+__device__ __forceinline__ void mma_ss4_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t acc0) {
+    if constexpr (F8) {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b32 alo, ahi, blo, bhi, x, y;\n\t.reg .b64 a, b;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "mov.b64 {alo, ahi}, %1;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t"
+            "add.u32 x, alo, %5;\n\tadd.u32 y, blo, %5;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, t;\n\t"
+            "add.u32 x, alo, %6;\n\tadd.u32 y, blo, %6;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, t;\n\t"
+            "add.u32 x, alo, %7;\n\tadd.u32 y, blo, %7;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, t;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b32 alo, ahi, blo, bhi, x, y;\n\t.reg .b64 a, b;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "mov.b64 {alo, ahi}, %1;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "add.u32 x, alo, %5;\n\tadd.u32 y, blo, %5;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+            "add.u32 x, alo, %6;\n\tadd.u32 y, blo, %6;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+            "add.u32 x, alo, %7;\n\tadd.u32 y, blo, %7;\n\tmov.b64 a, {x, ahi};\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
+            : "memory");
+    }
+}
+
+template <uint32_t ACOLS, uint32_t STEP, bool F8 = false>
+__device__ __forceinline__ void mma_ts4_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t acc0) {
+    if constexpr (F8) {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b32 blo, bhi, x, y;\n\t.reg .b64 b;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t"
+            "add.u32 x, %1, %5;\n\tadd.u32 y, blo, %8;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [x], b, %3, t;\n\t"
+            "add.u32 x, %1, %6;\n\tadd.u32 y, blo, %9;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [x], b, %3, t;\n\t"
+            "add.u32 x, %1, %7;\n\tadd.u32 y, blo, %10;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [x], b, %3, t;\n\t}"
+            ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc0), "n"(ACOLS), "n"(2 * ACOLS),
+              "n"(3 * ACOLS), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b32 blo, bhi, x, y;\n\t.reg .b64 b;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "setp.eq.b32 t, %4, %4;\n\t"
+            "mov.b64 {blo, bhi}, %2;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+            "add.u32 x, %1, %5;\n\tadd.u32 y, blo, %8;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+            "add.u32 x, %1, %6;\n\tadd.u32 y, blo, %9;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t"
+            "add.u32 x, %1, %7;\n\tadd.u32 y, blo, %10;\n\tmov.b64 b, {y, bhi};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x], b, %3, t;\n\t}"
+            ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc0), "n"(ACOLS), "n"(2 * ACOLS),
+              "n"(3 * ACOLS), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
+            : "memory");
+    }
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
