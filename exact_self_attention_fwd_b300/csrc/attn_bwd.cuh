@@ -346,17 +346,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const uint32_t col = C::COL_BUF * h;
             const uint64_t a0d = ptx::sdesc_sw128(a0, 16, 1024), a1d = ptx::sdesc_sw128(a1, 16, 1024);
             const uint64_t b0d = ptx::sdesc_sw128(b0, 16, 1024), b1d = ptx::sdesc_sw128(b1, 16, 1024);
+            // four K steps of 32 bytes per 128-byte swizzled slab, one asm statement each
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t aoff = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                const uint32_t boff = ((kk >> 2) * C::HCHUNK_BYTES + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_elect(tmem + col + C::COL_S, a0d + aoff, b0d + boff, IDESC_S, kk > 0 ? 1u : 0u);
+            for (int g = 0; g < D / 64; ++g) {
+                const uint64_t aoff = static_cast<uint64_t>(g * C::CHUNK_BYTES) >> 4;
+                const uint64_t boff = static_cast<uint64_t>(g * C::HCHUNK_BYTES) >> 4;
+                ptx::mma_ss4_elect<2>(tmem + col + C::COL_S, a0d + aoff, b0d + boff, IDESC_S, g > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t aoff = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                const uint32_t boff = ((kk >> 2) * C::HCHUNK_BYTES + (kk & 3) * 32) >> 4;
-                ptx::mma_ss_elect(tmem + col + C::COL_DP, a1d + aoff, b1d + boff, IDESC_S, kk > 0 ? 1u : 0u);
+            for (int g = 0; g < D / 64; ++g) {
+                const uint64_t aoff = static_cast<uint64_t>(g * C::CHUNK_BYTES) >> 4;
+                const uint64_t boff = static_cast<uint64_t>(g * C::HCHUNK_BYTES) >> 4;
+                ptx::mma_ss4_elect<2>(tmem + col + C::COL_DP, a1d + aoff, b1d + boff, IDESC_S, g > 0 ? 1u : 0u);
             }
             ptx::mma_commit_elect(bar(C::B_SDP + h));
         };
@@ -364,10 +365,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // packed columns), B = a streamed [64 x d] half tile read MN-major
         auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, bool accumulate) {
             const uint64_t bd = ptx::sdesc_sw128(b_addr, C::HCHUNK_BYTES, 1024);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4)
-                ptx::mma_ts_elect(tmem + col_d, tmem + col_a + k4 * 8, bd + ((k4 * 2048) >> 4), IDESC_ACC,
-                                  (accumulate || k4 > 0) ? 1u : 0u);
+            // four K steps of 16 rows (8 packed columns of A, 2048 bytes of B) in one asm statement
+            ptx::mma_ts4_elect<8, 128>(tmem + col_d, tmem + col_a, bd, IDESC_ACC, accumulate ? 1u : 0u);
         };
         // the accumulating products of sub-step h (half tile at hb), once the compute warps
         // wrote its P / dS
