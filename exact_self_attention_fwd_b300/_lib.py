@@ -368,8 +368,9 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, wi
 def attn_fwd_host(hq, hk, hv, ho, hlse, dq, dk, dv, do, dlse, causal: bool = False,
                   window: int = 0, scale: float | None = None, stream=None):
     """Host-buffer entry: copies hq/hk/hv into dq/dk/dv, runs, copies do/dlse back into
-    ho/hlse, all queued on `stream`. Host tensors should be pinned; synchronise the
-    stream before reading ho and hlse."""
+    ho/hlse, pipelined over chunks of (batch, KV head) groups so that copies overlap the
+    kernels (the copies run on two library-owned streams, ordered against `stream`).
+    Host tensors should be pinned; synchronise `stream` before reading ho and hlse."""
     import torch
     B, Hq, Hkv, N, d = _check_tensors(hq, hk, hv)
     _check_tensors(dq, dk, dv)

@@ -1248,6 +1248,16 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Streams and events of attn_fwd_host's copy pipeline, created once per device on the
+// first call and kept until the process exits.
+constexpr int HOST_CHUNKS = 8;
+struct HostPipe {
+    std::mutex mu;               // one enqueue sequence at a time
+    cudaStream_t h2d, d2h;       // non-blocking: no implicit ordering with the legacy stream
+    cudaEvent_t start, done, in[HOST_CHUNKS], out[HOST_CHUNKS];
+};
+HostPipe *g_host_pipe[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
 
 int cuda_fail(cudaError_t e) {
@@ -1506,6 +1516,31 @@ int noalloc_scratch(void **out) {
         g_scratch_addr[dev] = ptr;
     }
     *out = g_scratch_addr[dev];
+    return ATTN_OK;
+}
+
+// attn_fwd_host's streams and events on the current device, created on first use
+int host_pipe(HostPipe **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_host_pipe[dev]) {
+        HostPipe *hp = new HostPipe();
+        const unsigned ev_flags = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp->start, ev_flags)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp->done, ev_flags)) != cudaSuccess)
+            return cuda_fail(e);
+        for (int c = 0; c < HOST_CHUNKS; ++c)
+            if ((e = cudaEventCreateWithFlags(&hp->in[c], ev_flags)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp->out[c], ev_flags)) != cudaSuccess)
+                return cuda_fail(e);
+        g_host_pipe[dev] = hp;
+    }
+    *out = g_host_pipe[dev];
     return ATTN_OK;
 }
 
@@ -1861,19 +1896,54 @@ int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, floa
     if (rc != ATTN_OK) return rc;
     rc = validate(hq, hk, hv, ho, hlse, B, Hq, Hkv, N, d, causal, window, scale);
     if (rc != ATTN_OK) return rc;
+    int sms = 0;
+    if ((rc = device_setup(&sms)) != ATTN_OK) return rc;
+    HostPipe *hp = nullptr;
+    if ((rc = host_pipe(&hp)) != ATTN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t q_bytes = static_cast<size_t>(B) * Hq * N * d * 2;
-    const size_t kv_bytes = static_cast<size_t>(B) * Hkv * N * d * 2;
-    const size_t lse_bytes = static_cast<size_t>(B) * Hq * N * sizeof(float);
+    // The (batch, KV head) groups are independent, and each is contiguous in every
+    // tensor: G query heads of q, o and lse, one head of k and v. Chunks of consecutive
+    // groups go through a three-stage pipeline: host-to-device copies on one
+    // library stream, the kernel on `stream`, device-to-host copies on a second library
+    // stream, so that the copies of one chunk overlap the kernel and the copies of
+    // the others. Each chunk is an attn_fwd call over its groups (one KV head each).
+    const int G = Hq / Hkv;
+    const long long groups = static_cast<long long>(B) * Hkv;
+    const int nchunks = static_cast<int>(groups < HOST_CHUNKS ? groups : HOST_CHUNKS);
+    const size_t q_g = static_cast<size_t>(G) * N * d * 2, kv_g = static_cast<size_t>(N) * d * 2;
+    const size_t lse_g = static_cast<size_t>(G) * N * sizeof(float);
+    auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
+    auto atw = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
+    // one enqueue sequence at a time on the shared library streams and events
+    std::lock_guard<std::mutex> lock(hp->mu);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(dq, hq, q_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dk, hk, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dv, hv, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess)
         return cuda_fail(e);
-    rc = attn_fwd(dq, dk, dv, do_, dlse, B, Hq, Hkv, N, d, causal, window, scale, stream);
-    if (rc != ATTN_OK) return rc;
-    if ((e = cudaMemcpyAsync(ho, do_, q_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(hlse, dlse, lse_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    for (int c = 0; c < nchunks; ++c) {
+        const long long g0 = groups * c / nchunks, g1 = groups * (c + 1) / nchunks;
+        const size_t ng = static_cast<size_t>(g1 - g0);
+        const size_t oq = static_cast<size_t>(g0) * q_g, okv = static_cast<size_t>(g0) * kv_g;
+        const size_t ol = static_cast<size_t>(g0) * lse_g;
+        if ((e = cudaMemcpyAsync(atw(dq, oq), at(hq, oq), ng * q_g, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(dk, okv), at(hk, okv), ng * kv_g, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(dv, okv), at(hv, okv), ng * kv_g, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->in[c], hp->h2d)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(s, hp->in[c], 0)) != cudaSuccess)
+            return cuda_fail(e);
+        rc = attn_fwd(atw(dq, oq), atw(dk, okv), atw(dv, okv), atw(do_, oq),
+                      reinterpret_cast<float *>(atw(dlse, ol)), static_cast<int>(ng), G, 1, N, d, causal, window,
+                      scale, stream);
+        if (rc != ATTN_OK) return rc;
+        if ((e = cudaEventRecord(hp->out[c], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(ho, oq), at(do_, oq), ng * q_g, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(atw(hlse, ol), at(dlse, ol), ng * lse_g, cudaMemcpyDeviceToHost, hp->d2h)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+    }
+    // `stream` completes only after the last device-to-host copy
+    if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess || (e = cudaStreamWaitEvent(s, hp->done, 0)) != cudaSuccess)
         return cuda_fail(e);
     return ATTN_OK;
 }

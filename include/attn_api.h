@@ -290,14 +290,22 @@ int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o
 /*
  * attn_fwd_host -- the same operation for callers whose tensors live in host memory.
  *
- * Queues on `stream`: one host-to-device copy each of q, k and v into the
- * caller-owned device buffers dq, dk, dv; the attn_fwd kernel writing do_ and dlse;
- * one device-to-host copy each of do_ and dlse into ho and hlse. Layouts, sizes and
- * alignment rules are those of attn_fwd, for both the host and the device buffers.
- * Host buffers should be page-locked (cudaHostAlloc / pinned) for the copies to be
- * asynchronous; with pageable memory CUDA stages them synchronously. The results
- * in ho and hlse are valid once `stream` has been synchronised. Nothing is
- * allocated.
+ * Copies q, k and v into the caller-owned device buffers dq, dk, dv, runs the forward
+ * writing do_ and dlse, and copies do_ and dlse back into ho and hlse. Layouts, sizes
+ * and alignment rules are those of attn_fwd, for both the host and the device buffers.
+ *
+ * The (batch, KV head) groups are independent, so the call is pipelined over up to 8
+ * chunks of consecutive groups: host-to-device copies on a library-owned stream, the
+ * kernel of each chunk on `stream`, device-to-host copies on a second library-owned
+ * stream, ordered by events, so that the copies of one chunk overlap the kernel and the
+ * copies of the others. The two streams and their events are created once per device,
+ * on the first call there, and kept until the process exits; nothing is allocated per
+ * call. Work queued on `stream` before the call is complete before the first copy, and
+ * `stream` reaches the end of the call only after the last copy, so the results in ho
+ * and hlse are valid once `stream` has been synchronised. Calls from several host
+ * threads are safe; their copies share the library streams. Host buffers should be
+ * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous; with pageable
+ * memory CUDA stages them synchronously.
  */
 int attn_fwd_host(const void *hq, const void *hk, const void *hv, void *ho, float *hlse,
                   void *dq, void *dk, void *dv, void *do_, float *dlse,

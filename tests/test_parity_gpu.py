@@ -181,6 +181,72 @@ def test_host_entry_matches_device_entry():
     assert torch.equal(ho, ref[0].cpu()) and torch.equal(hl, ref[1].cpu())
 
 
+def _host_call(q, k, v, causal, window, scale, stream=None, keep=None):
+    """The copies are asynchronous: the pinned inputs must outlive them (until the
+    stream is synchronised), so they are appended to `keep`, or to a module list."""
+    B, Hq, N, d = q.shape
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty_like(q).pin_memory()
+    hl = torch.empty(B, Hq, N, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q, device=DEV), torch.empty_like(k, device=DEV), torch.empty_like(v, device=DEV)
+    do = torch.empty_like(q, device=DEV)
+    dl = torch.empty(B, Hq, N, dtype=torch.float32, device=DEV)
+    ea.attn_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do, dl, causal=causal, window=window, scale=scale,
+                     stream=stream)
+    (_PINNED if keep is None else keep).extend([hq, hk, hv])
+    return ho, hl, (dq, dk, dv, do, dl)
+
+
+_PINNED = []
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d", [(3, 10, 5, 260, 64), (1, 4, 1, 300, 128), (2, 16, 8, 129, 128)])
+def test_host_entry_chunks(B, Hq, Hkv, N, d):
+    # 15 groups over 8 chunks (uneven), a single group, 16 groups over 8 chunks: the
+    # pipelined host entry gives the device entry's bits
+    q, k, v = make_qkv(B, Hq, Hkv, N, d, 12 + B + Hkv)
+    ref = run_gpu(q, k, v, True, 0, 0.1)
+    ho, hl, _ = _host_call(q, k, v, True, 0, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(ho, ref[0].cpu()) and torch.equal(hl, ref[1].cpu())
+
+
+def test_host_entry_back_to_back_and_threads():
+    # two calls in a row reusing the same device buffers, then two host threads at
+    # once on two streams: every result equals its own device-entry result
+    import threading
+    cases = [make_qkv(2, 8, 2, 700, 128, 30 + i) for i in range(3)]
+    refs = [run_gpu(q, k, v, True, 0, 0.09) for q, k, v in cases]
+    q, k, v = cases[0]
+    ho, hl, bufs = _host_call(q, k, v, True, 0, 0.09)
+    q2, k2, v2 = cases[1]
+    hq2, hk2, hv2 = q2.pin_memory(), k2.pin_memory(), v2.pin_memory()
+    ho2 = torch.empty_like(q2).pin_memory()
+    hl2 = torch.empty(2, 8, 700, dtype=torch.float32).pin_memory()
+    ea.attn_fwd_host(hq2, hk2, hv2, ho2, hl2, *bufs, causal=True, window=0, scale=0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(ho, refs[0][0].cpu()) and torch.equal(hl, refs[0][1].cpu())
+    assert torch.equal(ho2, refs[1][0].cpu()) and torch.equal(hl2, refs[1][1].cpu())
+    out = {}
+
+    def worker(i):
+        torch.cuda.set_device(0)
+        st = torch.cuda.Stream()
+        qq, kk, vv = cases[i]
+        with torch.cuda.stream(st):
+            out[i] = _host_call(qq, kk, vv, True, 0, 0.09, stream=st)[:2]
+        st.synchronize()
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in (1, 2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    torch.cuda.synchronize()
+    for i in (1, 2):
+        assert torch.equal(out[i][0], refs[i][0].cpu()) and torch.equal(out[i][1], refs[i][1].cpu())
+
+
 def test_output_buffers_untouched_outside_shape():
     # the kernel writes exactly B*Hq*N rows: a guard region after O and LSE stays intact
     q, k, v = make_qkv(1, 2, 2, 197, 64, 11)
