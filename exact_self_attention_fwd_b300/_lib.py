@@ -6,6 +6,7 @@ refuses tensors that are not CUDA bf16/fp32 of the required shape.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -24,6 +25,8 @@ ATTN_ERR_CUDA = -5
 ATTN_ERR_TIMEOUT = -6
 ATTN_ERR_WORKSPACE = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
+ATTN_ERR_BOUNDS = -9
+DEBUG_LIB_PATH = os.path.join(PKG, "libattn_fwd_debug.so")
 
 _lib = None
 
@@ -80,6 +83,12 @@ def _declare(lib):
     lib.attn_selftest_wait_timeout.restype = i
     lib.attn_version.argtypes = []
     lib.attn_version.restype = i
+    lib.attn_debug_build.argtypes = []
+    lib.attn_debug_build.restype = i
+    lib.attn_debug_first_site.argtypes = [i]
+    lib.attn_debug_first_site.restype = i
+    lib.attn_debug_selftest.argtypes = []
+    lib.attn_debug_selftest.restype = i
     return lib
 
 
@@ -95,6 +104,19 @@ def load(path: str | None = None):
                 " (there is no fallback implementation)")
         _lib = _declare(ctypes.CDLL(LIB_PATH))
     return _lib
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Route this module's wrappers through another build of the library (for
+    example the debug build, load(DEBUG_LIB_PATH)) inside a `with` block."""
+    global _lib
+    old = _lib
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = old
 
 
 def status_str(code: int) -> str:

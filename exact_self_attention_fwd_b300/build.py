@@ -19,6 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn_fwd.so")
+DEBUG_LIB = os.path.join(PKG, "libattn_fwd_debug.so")  # index-checked build (ATTN_DEBUG)
 SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "attn_bwd.cuh"),
                   os.path.join(INCLUDE, "attn_api.h")]
@@ -48,10 +49,11 @@ def _split_constants() -> dict:
     return out
 
 
-def check_registers(ptxas_log: str) -> None:
+def check_registers(ptxas_log: str, allow_spills: bool = False) -> None:
     """The forward kernels launch at a fixed register count and then move registers
     between warpgroups with setmaxnreg; the split must fit in the launch allocation
-    and nothing may spill. Refuse the build otherwise."""
+    and nothing may spill (the index-checked debug build may). Refuse the build
+    otherwise."""
     k = _split_constants()
     need = 2 * 128 * k["SOFTMAX_REGS"] + 128 * k["PRODUCER_REGS"]
     blocks = re.split(r"Compiling entry function", ptxas_log)
@@ -60,7 +62,7 @@ def check_registers(ptxas_log: str) -> None:
         head = blk.split("\n", 1)[0]
         if "attn_bwd_kernel" in head:
             spill = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", blk)
-            if spill and (int(spill.group(1)) or int(spill.group(2))):
+            if spill and (int(spill.group(1)) or int(spill.group(2))) and not allow_spills:
                 raise RuntimeError("backward kernel spills registers:\n" + blk)
             continue
         if "attn_fwd_kernel" not in head:
@@ -70,22 +72,26 @@ def check_registers(ptxas_log: str) -> None:
         spill = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", blk)
         if regs * k["NUM_THREADS"] < need:
             raise RuntimeError(f"register split {need} exceeds launch allocation {regs} x {k['NUM_THREADS']}")
-        if spill and (int(spill.group(1)) or int(spill.group(2))):
+        if spill and (int(spill.group(1)) or int(spill.group(2))) and not allow_spills:
             raise RuntimeError("forward kernel spills registers:\n" + blk)
     if seen == 0:
         raise RuntimeError("ptxas output did not list the forward kernels")
 
 
-def build(force: bool = False, verbose: bool = False, out: str = LIB) -> str:
+def build(force: bool = False, verbose: bool = False, out: str | None = None, debug: bool = False) -> str:
+    """Compile the library (or, debug=True, its index-checked build) in-tree."""
+    out = out or (DEBUG_LIB if debug else LIB)
     if not force and up_to_date(out):
         return out
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-cudart", "static", "-I", INCLUDE, "-I", CSRC, "-o", out + ".tmp", *SOURCES]
+    if debug:
+        cmd += ["-DATTN_DEBUG"]
     cmd += ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    check_registers(res.stdout + res.stderr)
+    check_registers(res.stdout + res.stderr, allow_spills=debug)
     if verbose:
         print(res.stdout + res.stderr)
     os.replace(out + ".tmp", out)
@@ -96,5 +102,6 @@ if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--force", action="store_true")
+    ap.add_argument("--debug", action="store_true", help="the index-checked build (libattn_fwd_debug.so)")
     a = ap.parse_args()
-    print(build(force=a.force or a.verbose, verbose=a.verbose))
+    print(build(force=a.force or a.verbose, verbose=a.verbose, debug=a.debug))

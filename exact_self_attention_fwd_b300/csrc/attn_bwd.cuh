@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (prow >= BH * N_pad) return;
+    if (!ATTN_CHECK(prow >= 0 && N <= N_pad, 25u)) return;
     const long long h = prow / N_pad;
     const int i = static_cast<int>(prow - h * N_pad);
     if (i >= N) {
@@ -282,6 +283,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ok = wait_warp(bar(C::B_FIXEMPTY), (fix_it & 1u) ^ 1u, abort_flag, limit);
             ++fix_it;
             if (!ok) break;
+            // debug build: the stationary tile's head and rows
+            if (!ATTN_CHECK(w.zfix >= 0 && w.zfix < p.B * (MODE == 0 ? p.Hkv : p.Hq) && w.tile >= 0 &&
+                                w.tile * BM < p.N,
+                            20u))
+                continue;
             ptx::mbar_arrive_expect_tx_elect(bar(C::B_FIXFULL), 2 * C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c) {
@@ -303,6 +309,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     ++hit;
                     const uint32_t dst = half_base(slot);
                     const int row0 = t * BM + 64 * h;
+                    // debug build: the ring half-slot, the streamed head and rows (and, for
+                    // dK/dV, the row terms read beside them)
+                    if (!ATTN_CHECK(slot < static_cast<uint32_t>(C::HSTAGES) && zs >= 0 &&
+                                        zs < p.B * (MODE == 0 ? p.Hq : p.Hkv) && row0 >= 0 && row0 + 64 <= p.N_pad,
+                                    21u))
+                        continue;
                     if constexpr (MODE == 0) {
                         // the half tile's 64 values of lse log2(e) and of D land beside it
                         const uint32_t vec = sb + C::SMEM_VEC + slot * C::VEC_BYTES;
@@ -344,6 +356,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // stationary 128-row tile, B the streamed 64-row half tile
         auto issue_sdp = [&](int h, uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1) {
             const uint32_t col = C::COL_BUF * h;
+            // debug build: S and dP of the sub-step inside tensor memory
+            if (!ATTN_CHECK(col + C::COL_DP + 64 <= TMEM_COLS && col + C::COL_S + 64 <= TMEM_COLS, 22u)) return;
             const uint64_t a0d = ptx::sdesc_sw128(a0, 16, 1024), a1d = ptx::sdesc_sw128(a1, 16, 1024);
             const uint64_t b0d = ptx::sdesc_sw128(b0, 16, 1024), b1d = ptx::sdesc_sw128(b1, 16, 1024);
             // four K steps of 32 bytes per 128-byte swizzled slab, one asm statement each
@@ -364,6 +378,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // D[tmem] (+)= A[tmem, bf16] B for one sub-step: A = 64 rows' worth of P / dS (32
         // packed columns), B = a streamed [64 x d] half tile read MN-major
         auto issue_acc = [&](uint32_t col_d, uint32_t col_a, uint32_t b_addr, bool accumulate) {
+            // debug build: the accumulator and the packed A operand inside tensor memory
+            if (!ATTN_CHECK(col_d + D <= TMEM_COLS && col_a + 32 <= TMEM_COLS, 23u)) return;
             const uint64_t bd = ptx::sdesc_sw128(b_addr, C::HCHUNK_BYTES, 1024);
             // four K steps of 16 rows (8 packed columns of A, 2048 bytes of B) in one asm statement
             ptx::mma_ts4_elect<8, 128>(tmem + col_d, tmem + col_a, bd, IDESC_ACC, accumulate ? 1u : 0u);
@@ -566,7 +582,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = 0u;
                 }
-                if (r_abs < p.N) {
+                // debug build: the gradient row inside its output
+                if (r_abs < p.N && ATTN_CHECK(w.zfix >= 0 && w.zfix < p.B * (MODE == 0 ? p.Hkv : p.Hq), 24u)) {
                     uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(w.zfix) * p.N + r_abs) * D + col0 +
                                                            32 * c);
 #pragma unroll

@@ -68,7 +68,26 @@ constexpr float LN2 = 0.693147180559945309f;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr uint32_t WAIT_SLEEP_NS = 200000u;  // a waiting thread re-checks at least this often
 
-__device__ unsigned int g_status;  // bit 0: some wait ran out of time
+__device__ unsigned int g_status;  // bit 0: some wait ran out of time; bit 1: an index check failed
+constexpr uint32_t STATUS_BOUNDS = 2u;
+
+// Index checks of the debug build (compiled with -DATTN_DEBUG). Each guards an access
+// whose index comes from the scheduling arithmetic: a shared-memory stage or buffer,
+// a tensor-memory column range, a tensor-map coordinate, a global row. A failed check
+// sets bit 1 of the status word and records the first failing site; the caller then
+// skips the access (a skipped copy leaves its barrier incomplete, and the bounded wait
+// behind it ends the kernel). In the release build every check is the constant true
+// and costs nothing.
+#ifdef ATTN_DEBUG
+__device__ unsigned int g_debug_site;
+__device__ __noinline__ void debug_fail(unsigned int site) {
+    atomicOr(&g_status, STATUS_BOUNDS);
+    atomicCAS(&g_debug_site, 0u, site);
+}
+#define ATTN_CHECK(cond, site) ((cond) ? true : (::attn::debug_fail(site), false))
+#else
+#define ATTN_CHECK(cond, site) true
+#endif
 
 // Scratch of attn_fwd_decode_noalloc: the per-split partial results that attn_fwd_decode
 // keeps in a caller-provided workspace live here instead, in a fixed array that every
@@ -265,6 +284,7 @@ __device__ __forceinline__ int snake_unit(int k) {
 // Valid length of batch b: key_len[b] clamped to [0, N], or N without padding.
 __device__ __forceinline__ int valid_len(const Params &p, int b) {
     if (!p.key_len) return p.N;
+    if (!ATTN_CHECK(b >= 0 && b < p.B, 8u)) return 0;
     return min(max(__ldg(p.key_len + b), 0), p.N);
 }
 
@@ -431,6 +451,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 ++q_it;
                 const uint32_t qdst = sb + C::SMEM_Q + qb * 2 * C::TILE_BYTES;
+                // debug build: the Q buffer and the tensor-map z index of the unit's rows
+                if (!ATTN_CHECK(qb < static_cast<uint32_t>(C::Q_BUFS) && zq >= 0 &&
+                                    zq < (DEC ? p.B * p.Hkv : p.B * p.Hq) && q0a >= 0 && q0a < p.N,
+                                1u))
+                    continue;
                 ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 2 * qb + 0), C::TILE_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::NCHUNK; ++c)
@@ -454,6 +479,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
                         ok = wait_warp(bar(C::B_KVEMPTY + st), ph, abort_flag, limit);
                         if (!ok) break;
+                        // debug build: the ring stage, the KV head and the key tile
+                        if (!ATTN_CHECK(st < static_cast<uint32_t>(C::STAGES) && zkv >= 0 && zkv < p.B * p.Hkv &&
+                                            j >= 0 && j * BN < p.Nk,
+                                        2u)) {
+                            ++kv_it;
+                            continue;
+                        }
                         ptx::mbar_arrive_expect_tx_elect(bar(C::B_KVFULL + st), C::TILE_BYTES);
                         const CUtensorMap *m = kv ? &tm_v : &tm_k;
 #pragma unroll
@@ -496,6 +528,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the MMA warp's instruction count per MMA bounds how fast it feeds the
             // tensor core).
             auto issue_s = [&](uint32_t qa, uint32_t col_s, uint32_t kslot) {
+                // debug build: the K stage, the Q tiles inside their region, S inside tensor memory
+                if (!ATTN_CHECK(kslot < static_cast<uint32_t>(C::STAGES) && qa >= sb + C::SMEM_Q &&
+                                    qa + C::TILE_BYTES <= sb + C::SMEM_KV && col_s + BN <= TMEM_COLS,
+                                3u))
+                    return;
                 const uint64_t qd = ptx::sdesc_sw128(qa, 16, 1024);
                 const uint64_t kd = ptx::sdesc_sw128(sb + C::SMEM_KV + kslot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
@@ -510,12 +547,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // is still being computed.
             auto issue_pv = [&](int t, uint32_t col_o, uint32_t col_s, uint32_t vslot,
                                 bool accumulate, uint32_t parity) -> bool {
+                // debug build: the V stage, O and P inside tensor memory
+                const bool in_range = ATTN_CHECK(vslot < static_cast<uint32_t>(C::STAGES) &&
+                                                     col_o + D <= TMEM_COLS && col_s + C::P_COLS <= TMEM_COLS,
+                                                 4u);
                 const uint64_t vd = ptx::sdesc_sw128(sb + C::SMEM_KV + vslot * C::TILE_BYTES,
                                                      C::CHUNK_BYTES, 1024);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     if (!wait_warp(bar(C::B_PFULL + 2 * t + h), parity, abort_flag, limit)) return false;
                     ptx::tc_fence_after();
+                    if (!in_range) continue;
                     // step k16 reads 8 tensor-memory columns of P (KSTEP keys) and the KSTEP
                     // rows of V after the previous steps' KSTEP * 128 bytes; a bf16 half is
                     // four steps, issued from one asm statement
@@ -681,6 +723,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_s = tmem + lane_off + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t t_o = tmem + lane_off + (t ? C::COL_O1 : C::COL_O0);
         const uint32_t t_p = tmem + lane_off + (t ? C::COL_P1 : C::COL_P0);
+        // debug build: S, O and P of this tile inside tensor memory (a failure is recorded;
+        // the layout is fixed at compile time)
+        (void)ATTN_CHECK((t ? C::COL_S1 : C::COL_S0) + BN <= TMEM_COLS && (t ? C::COL_O1 : C::COL_O0) + D <= TMEM_COLS &&
+                             (t ? C::COL_P1 : C::COL_P0) + C::P_COLS <= TMEM_COLS,
+                         5u);
         // decode shape: tile row r holds query r % Nq (of head r / Nq of the group)
         int my_dec_pos = 0;
         if constexpr (DEC) my_dec_pos = p.pos_off + (row - fdiv(row, p.div_nq) * p.Nq);
@@ -711,7 +758,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // (P' = P x v_scale_j / v_max <= 256), so that O = v_max x sum P' V8 / sum P
             float q_sc = 1.f, v_max = 1.f;
             if constexpr (F8) {
-                q_sc = __ldg(p.q_scale + static_cast<size_t>(ui.zq) * p.n_kv + (q0 / BM));
+                // debug build: the query block's scale lies inside the scale array
+                if (ATTN_CHECK(ui.zq < p.B * p.Hq && q0 / BM < p.n_kv, 9u))
+                    q_sc = __ldg(p.q_scale + static_cast<size_t>(ui.zq) * p.n_kv + (q0 / BM));
                 float vm = 0.f;
                 for (int jj = lane; jj < p.n_kv; jj += 32)
                     vm = fmaxf(vm, __ldg(p.v_scale + static_cast<size_t>(ui.zkv) * p.n_kv + jj));
@@ -918,8 +967,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
                 if (p.o32) o32_row = p.o32 + ridx * D;
             }
+            // debug build: the row lies inside the output (or the split results) it is written to
+            const size_t rows_out = static_cast<size_t>(DEC ? p.B * p.Hkv : p.B * p.Hq) * static_cast<size_t>(p.N) *
+                                    static_cast<size_t>(DEC && p.splits > 1 ? p.splits : 1);
             if (o32_row) {
-                const bool store_row = qi < p.N;
+                const bool store_row = qi < p.N && ATTN_CHECK(lse_idx < rows_out, 6u);
                 float4 *dst = reinterpret_cast<float4 *>(o32_row);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -947,6 +999,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // each thread writes its own row (2d contiguous bytes; rows past N are
             // skipped). The tensor-memory loads are warp-collective, so every lane takes
             // them.
+            const bool store_row = qi < p.N && ATTN_CHECK(ridx < rows_out, 7u);
             {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D);
 #pragma unroll 1
@@ -959,7 +1012,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = 0u;
                     }
-                    if (qi < p.N) {
+                    if (store_row) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             uint4 val;
@@ -977,7 +1030,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            if (qi < p.N) p.lse[ridx] = lse_nat;
+            if (store_row) p.lse[ridx] = lse_nat;
         }
     }
 
@@ -1002,6 +1055,7 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16 
     constexpr int GROUPS = BM * D / 8 / 256;  // 8-element groups per thread
     const int blk = blockIdx.x, h = blockIdx.y;
     const int r0 = blk * BM;
+    if (!ATTN_CHECK(r0 < N && blk < nblk, 40u)) return;
     const int n = min(BM, N - r0) * D;  // elements in this block
     const size_t base = (static_cast<size_t>(h) * N + r0) * D;
     uint4 v[GROUPS];
@@ -1168,6 +1222,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
     const int row = blockIdx.x * 8 + static_cast<int>(threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
+    if (!ATTN_CHECK(row >= 0 && splits >= 1, 30u)) return;
     float m = -INFINITY;
     for (int s = lane; s < splits; s += 32) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
 #pragma unroll
@@ -1209,6 +1264,14 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
     for (int c = 0; c < PER / 2; ++c) dst[c] = ptx::pack_bf16x2(acc[2 * c], acc[2 * c + 1]);
     if (lane == 0) lse[row] = lse_row;
 }
+
+#ifdef ATTN_DEBUG
+// One failed check at site 99 (nothing is accessed): exercises the debug build's
+// reporting path.
+__global__ void debug_selftest_kernel() {
+    if (threadIdx.x == 0) (void)ATTN_CHECK(false, 99u);
+}
+#endif
 
 // One warp waits on a barrier nothing will complete; exercises the timeout path.
 __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
@@ -1987,6 +2050,7 @@ const char *attn_status_str(int status) {
         case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: the workspace is smaller than required";
         case ATTN_ERR_SCRATCH_LIMIT:
             return "ATTN_ERR_SCRATCH_LIMIT: the split results need more than the fixed 8 MiB scratch";
+        case ATTN_ERR_BOUNDS: return "ATTN_ERR_BOUNDS: an index check of the debug build failed";
         default: return "unknown attn_status";
     }
 }
@@ -2002,7 +2066,47 @@ int attn_device_error(int clear) {
         const unsigned int zero = 0;
         if ((e = cudaMemcpyToSymbol(attn::g_status, &zero, sizeof zero)) != cudaSuccess) return cuda_fail(e);
     }
+    if (word & attn::STATUS_BOUNDS) return ATTN_ERR_BOUNDS;
     return (word & attn::STATUS_TIMEOUT) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+int attn_debug_build(void) {
+#ifdef ATTN_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int attn_debug_first_site(int clear) {
+#ifdef ATTN_DEBUG
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int site = 0;
+    if ((e = cudaMemcpyFromSymbol(&site, attn::g_debug_site, sizeof site)) != cudaSuccess) return cuda_fail(e);
+    if (clear) {
+        const unsigned int zero = 0;
+        if ((e = cudaMemcpyToSymbol(attn::g_debug_site, &zero, sizeof zero)) != cudaSuccess) return cuda_fail(e);
+    }
+    return static_cast<int>(site);
+#else
+    (void)clear;
+    return 0;
+#endif
+}
+
+int attn_debug_selftest(void) {
+#ifdef ATTN_DEBUG
+    int sms = 0;
+    int rc = device_setup(&sms);
+    if (rc != ATTN_OK) return rc;
+    attn::debug_selftest_kernel<<<1, 32>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+#else
+    return ATTN_ERR_UNSUPPORTED;
+#endif
 }
 
 int attn_selftest_wait_timeout(int64_t limit_ns) {

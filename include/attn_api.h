@@ -68,8 +68,9 @@ typedef enum {
     ATTN_ERR_CUDA = -5,        /* a CUDA runtime call failed; see attn_last_cuda_error */
     ATTN_ERR_TIMEOUT = -6,     /* a kernel wait gave up (reported by attn_device_error) */
     ATTN_ERR_WORKSPACE = -7,   /* the caller's workspace is smaller than required */
-    ATTN_ERR_SCRATCH_LIMIT = -8 /* attn_fwd_decode_noalloc: the split results would need more
+    ATTN_ERR_SCRATCH_LIMIT = -8, /* attn_fwd_decode_noalloc: the split results would need more
                                    than its fixed scratch (ATTN_DECODE_NOALLOC_SCRATCH_BYTES) */
+    ATTN_ERR_BOUNDS = -9        /* debug build only: an index check failed (attn_device_error) */
 } attn_status;
 
 /*
@@ -324,10 +325,32 @@ int attn_last_cuda_error(void);
  * kernel of this library on it has given up a wait since the last clear: every
  * pipeline wait inside the kernels is bounded (2 s); a wait that runs out sets a
  * device-side status word, makes the kernel drain its own copies in flight, free
- * its tensor memory and return. Returns ATTN_OK, ATTN_ERR_TIMEOUT, or
- * ATTN_ERR_CUDA. clear != 0 resets the word after reading it.
+ * its tensor memory and return. Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BOUNDS
+ * (debug build: an index check failed; takes precedence), or ATTN_ERR_CUDA.
+ * clear != 0 resets the word after reading it.
  */
 int attn_device_error(int clear);
+
+/*
+ * The debug build (libattn_fwd_debug.so, compiled with ATTN_DEBUG defined) has the
+ * same entry points and results. Its kernels check the indices that the scheduling
+ * arithmetic produces before each access: shared-memory stages and buffers, tensor-
+ * memory column ranges, tensor-map coordinates, global rows written and per-batch or
+ * per-block values read. A failed check skips the access and records the failure
+ * instead of faulting: attn_device_error then returns ATTN_ERR_BOUNDS. No page
+ * describes this; it stands in for a memory checker, to run the test shapes under.
+ *
+ * attn_debug_build     1 in the debug build, 0 in the release build.
+ * attn_debug_first_site  synchronises, returns the number of the first check that
+ *                      failed since the last clear (0: none; always 0 in the release
+ *                      build), or ATTN_ERR_CUDA; clear != 0 resets it.
+ * attn_debug_selftest  debug build: queues one kernel whose only action is a failed
+ *                      check at site 99 (nothing is accessed), to test the reporting;
+ *                      ATTN_ERR_UNSUPPORTED in the release build.
+ */
+int attn_debug_build(void);
+int attn_debug_first_site(int clear);
+int attn_debug_selftest(void);
 
 /*
  * attn_selftest_wait_timeout -- exercises the bounded-wait failure path without a

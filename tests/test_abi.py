@@ -32,8 +32,21 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
+def test_debug_build_exports_every_declared_symbol():
+    # the index-checked build is a drop-in replacement: same exported entry points
+    from exact_self_attention_fwd_b300 import build
+    build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.DEBUG_LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in ea.header_functions():
+        assert n in exported, f"{n} declared in attn_api.h but not exported by the debug build"
+    dbg = ea.load(_lib.DEBUG_LIB_PATH)
+    assert dbg.attn_debug_build() == 1 and ea.load().attn_debug_build() == 0
+
+
 def test_status_strings(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = lib.attn_status_str(code).decode()
         assert s.startswith("ATTN_")
     assert lib.attn_status_str(-99).decode() == "unknown attn_status"
