@@ -352,7 +352,11 @@ def roofline_of(w: Workload, seconds_per_call: float, peaks: dict) -> dict:
     """The bound that limits workload w on this chip and the fraction of it achieved.
 
     Long sequences are tensor-core bound (FLOP/byte far above the ridge); the
-    short-sequence bidirectional workload is HBM bound."""
+    short-sequence bidirectional workload is HBM bound; the one-tile workload is bound
+    by launch latency (its microseconds per call are the figure, no fraction)."""
+    if w.name == "tiny":
+        return {"bound": "latency", "achieved": seconds_per_call * 1e6, "peak": None, "unit": "us per call",
+                "frac": None}
     if w.name == "vit_base":
         achieved = hbm_bytes(w) / seconds_per_call / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -819,7 +823,8 @@ def main(argv=None):
                     help="total oracle seconds for --impl reference")
     ap.add_argument("--summary-steps", type=int, default=100,
                     help="calls per workload for the all-workload summary (0 = skip)")
-    ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
+    ap.add_argument("--out-dir", default=os.path.join(ROOT, "bench_out"),
+                    help="where the nvidia-smi clock samples are written")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -151,3 +151,16 @@ def test_kernel_sha_covers_the_forward_kernel_only(tmp_path, monkeypatch):
     assert bench.kernel_sha() != base
     cu.write_text(src)
     assert bench.kernel_sha() == base
+
+
+def test_roofline_labels():
+    # the one-tile workload is launch-latency bound: its figure is microseconds per
+    # call, with no fraction of a throughput peak; the others report a fraction
+    import bench
+    from exact_self_attention_fwd_b300.inputs import WORKLOADS
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1700.0, "bf16_tflops_sustained": 1400.0}
+    r = bench.roofline_of(WORKLOADS["tiny"], 5e-6, peaks)
+    assert r["bound"] == "latency" and r["frac"] is None and abs(r["achieved"] - 5.0) < 1e-9
+    assert bench.roofline_of(WORKLOADS["vit_base"], 1e-4, peaks)["bound"] == "hbm"
+    r = bench.roofline_of(WORKLOADS["gqa_8k"], 7e-4, peaks)
+    assert r["bound"] == "tensor" and 0 < r["frac"] < 1.5
