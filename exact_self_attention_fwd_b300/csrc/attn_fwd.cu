@@ -650,6 +650,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mma_commit_elect(bar(C::B_QEMPTY + qb));  // Q tiles free once the last S is done
                     ok = pv_step(prev);
                     if (!ok) break;
+                } else if (has1 && ui.lo1 == lo0 + 1 && ui.hi1 == hi0 + 1) {
+                    // A sliding window: tile 1's key range is tile 0's shifted by one tile.
+                    // Tile 1 runs one key tile ahead, so both tiles compute in every step
+                    // (n steps instead of n + 1, with no step for one tile alone): step j
+                    // does O0 += P0 V(j-1), S0 = Q0 K(j)^T, O1 += P1 V(j), S1 = Q1 K(j+1)^T.
+                    // Each K/V tile is waited for right before its first use (the ring
+                    // refills while the earlier products of the step run) and released
+                    // after its last. The producer's order is unchanged: K, V of key tiles
+                    // lo0 .. hi0.
+                    const uint32_t base = kv_it;
+                    kv_it += 2u * static_cast<uint32_t>(hi - lo);
+                    auto kv_slot = [&](int j, uint32_t kv) {
+                        return (base + 2u * static_cast<uint32_t>(j - lo0) + kv) % C::STAGES;
+                    };
+                    auto kv_wait = [&](int j, uint32_t kv) -> bool {
+                        const uint32_t it = base + 2u * static_cast<uint32_t>(j - lo0) + kv;
+                        if (!wait_warp(bar(C::B_KVFULL + it % C::STAGES), (it / C::STAGES) & 1u, abort_flag, limit))
+                            return false;
+                        ptx::tc_fence_after();
+                        return true;
+                    };
+                    ok = kv_wait(lo0, 0);
+                    for (int j = lo0; ok && j < hi0; ++j) {
+                        if (j > lo0) {
+                            if (j - 1 == lo0) ok = kv_wait(lo0, 1);  // V(lo0): tile 1 never reads it
+                            if (ok) ok = issue_pv(0, C::COL_O0, C::COL_P0, kv_slot(j - 1, 1), j - 1 > lo0, p_use0 & 1u);
+                            ++p_use0;
+                            if (!ok) break;
+                            ptx::mma_commit_elect(bar(C::B_KVEMPTY + kv_slot(j - 1, 1)));
+                        }
+                        issue_s(qa0, C::COL_S0, kv_slot(j, 0));
+                        ptx::mma_commit_elect(bar(C::B_SFULL + 0));
+                        ptx::mma_commit_elect(bar(C::B_KVEMPTY + kv_slot(j, 0)));
+                        if (j > lo0) {
+                            ok = kv_wait(j, 1) &&
+                                 issue_pv(1, C::COL_O1, C::COL_P1, kv_slot(j, 1), j > lo0 + 1, p_use1 & 1u);
+                            ++p_use1;
+                            if (!ok) break;
+                        }
+                        ok = kv_wait(j + 1, 0);
+                        if (!ok) break;
+                        issue_s(qa1, C::COL_S1, kv_slot(j + 1, 0));
+                        ptx::mma_commit_elect(bar(C::B_SFULL + 1));
+                        if (j + 1 >= hi0) ptx::mma_commit_elect(bar(C::B_KVEMPTY + kv_slot(j + 1, 0)));
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit_elect(bar(C::B_QEMPTY + qb));  // Q tiles free once the last S is done
+                    // the last products: O0 += P0 V(hi0-1), O1 += P1 V(hi0)
+                    if (hi0 - 1 == lo0) ok = kv_wait(lo0, 1);
+                    if (ok) ok = issue_pv(0, C::COL_O0, C::COL_P0, kv_slot(hi0 - 1, 1), hi0 - 1 > lo0, p_use0 & 1u);
+                    ++p_use0;
+                    if (!ok) break;
+                    ptx::mma_commit_elect(bar(C::B_OFULL + 0));
+                    ptx::mma_commit_elect(bar(C::B_KVEMPTY + kv_slot(hi0 - 1, 1)));
+                    ok = kv_wait(hi0, 1) && issue_pv(1, C::COL_O1, C::COL_P1, kv_slot(hi0, 1), hi0 > lo0 + 1, p_use1 & 1u);
+                    ++p_use1;
+                    if (!ok) break;
+                    ptx::mma_commit_elect(bar(C::B_OFULL + 1));
+                    ptx::mma_commit_elect(bar(C::B_KVEMPTY + kv_slot(hi0, 1)));
                 } else {
                     for (int j = lo; j < hi; ++j) {
                         const uint32_t ks = kv_it % C::STAGES, kph = (kv_it / C::STAGES) & 1u;
