@@ -139,6 +139,10 @@ struct Params {
     // decode shape: query tiles pack the G * Nq rows of one KV head (N = G * Nq rows
     // per tensor-map z index); unit = (batch * Hkv + hkv, split of the key tiles)
     int Nq, splits, split_lo, split_len, split_hi;
+    // decode shape with both query tiles on one split (at most 32 packed rows): tile 0
+    // takes the split's even key tiles, tile 1 the odd ones, over the same packed rows;
+    // tile 1 hands its result to tile 0 through shared memory, which merges the two
+    int dec2;
     FastDiv div_splits, div_nq;
     float *o_part, *lse_part;  // partial results per split (splits > 1), fp32
     float *o32;                // plain forward: O as fp32 instead of bf16 (null: bf16 to o)
@@ -147,7 +151,9 @@ struct Params {
 };
 
 // F8: Q, K and V are e4m3 codes (1 byte) instead of bf16 (2 bytes); O stays bf16.
-template <int D, bool F8 = false>
+// DEC: the decode shape, which loads no Q for tile 1 and has room for a fifth stage at
+// d = 128.
+template <int D, bool F8 = false, bool DEC = false>
 struct Cfg {
     static constexpr int ELEM = F8 ? 1 : 2;                 // bytes per Q/K/V element
     static constexpr int KSTEP = F8 ? 32 : 16;              // reduction length of one MMA
@@ -155,7 +161,7 @@ struct Cfg {
     static constexpr int CHUNK_BYTES = BM * 128;            // one slab: 128 rows x 128 bytes
     static constexpr int NCHUNK = D / CHUNK_COLS;
     static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
-    static constexpr int STAGES = (D == 128 && !F8) ? 4 : 8;
+    static constexpr int STAGES = (D == 128 && !F8) ? (DEC ? 5 : 4) : 8;
     // Q tiles of Q_BUFS units: with two, the producer loads the next unit's Q while the
     // current unit still computes (where shared memory has room for it).
     static constexpr int Q_BUFS = (D == 64 || F8) ? 2 : 1;
@@ -172,7 +178,9 @@ struct Cfg {
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
     static constexpr int B_PVDONE = B_SFREE + 2;    // 2: a P.V product of tile t completed
-    static constexpr int B_DRAIN = B_PVDONE + 2;    // 1
+    static constexpr int B_XFULL = B_PVDONE + 2;    // 1: decode, tile 1's result is in shared memory
+    static constexpr int B_XEMPTY = B_XFULL + 1;    // 1: decode, tile 0 has merged it
+    static constexpr int B_DRAIN = B_XEMPTY + 1;    // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_CTL + 16;
@@ -188,6 +196,10 @@ struct Cfg {
     static constexpr int P_COLS = BN * ELEM / 4;
     static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
     static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
+    // decode: tile 1's normalised O (fp32, [32][D]) and LSE ([32]) for tile 0 to merge,
+    // in the second Q slot of buffer 0, which the decode shape never loads
+    static constexpr int SMEM_XCHG = SMEM_Q + TILE_BYTES;
+    static_assert(!DEC || 32 * D * 4 + 32 * 4 <= TILE_BYTES, "decode exchange buffer");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
@@ -361,6 +373,12 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const Params &p) {
         ui.hi0 = min(ui.lo0 + p.split_len, p.split_hi);
         if (ui.hi0 <= ui.lo0) ui.lo0 = ui.hi0 = 0;  // nothing left for this split
         ui.lo1 = ui.hi1 = 0;
+        // both tiles on the split: tile 0 from the first key tile, tile 1 from the second,
+        // each taking every other tile up to hi
+        if (p.dec2 && ui.hi0 > ui.lo0 + 1) {
+            ui.lo1 = ui.lo0 + 1;
+            ui.hi1 = ui.hi0;
+        }
     }
     return ui;
 }
@@ -372,7 +390,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const Params p) {
-    using C = Cfg<D, F8>;
+    using C = Cfg<D, F8, DEC>;
     static_assert(!F8 || (D == 128 && !DEC), "e4m3 operands: d = 128, plain forward");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -403,6 +421,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(C::B_SFREE + t), 4);
             ptx::mbar_init(bar(C::B_PVDONE + t), 1);
         }
+        ptx::mbar_init(bar(C::B_XFULL), 1);
+        ptx::mbar_init(bar(C::B_XEMPTY), 1);
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
         ptx::fence_barrier_init();
@@ -461,38 +481,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int c = 0; c < C::NCHUNK; ++c)
                     ptx::tma_load_3d_elect(qdst + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + 2 * qb + 0),
                                            c * C::CHUNK_COLS, q0a, zq);
-                if (has1) {
+                if (has1 && !DEC) {
                     ptx::mbar_arrive_expect_tx_elect(bar(C::B_QFULL + 2 * qb + 1), C::TILE_BYTES);
 #pragma unroll
                     for (int c = 0; c < C::NCHUNK; ++c)
                         ptx::tma_load_3d_elect(qdst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q,
                                                bar(C::B_QFULL + 2 * qb + 1), c * C::CHUNK_COLS, q0b, zq);
                 } else if (lane == 0) {
-                    // no second tile: complete the phase anyway, so that both barriers of a
-                    // buffer always advance together
+                    // no second tile (or the decode shape, whose second tile reads the first
+                    // tile's Q): complete the phase anyway, so that both barriers of a buffer
+                    // always advance together
                     ptx::mbar_arrive(bar(C::B_QFULL + 2 * qb + 1));
                 }
-                for (int j = lo; ok && j < hi; ++j) {
-#pragma unroll 1
-                    for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
-                        const uint32_t st = kv_it % C::STAGES;
-                        const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
-                        ok = wait_warp(bar(C::B_KVEMPTY + st), ph, abort_flag, limit);
-                        if (!ok) break;
-                        // debug build: the ring stage, the KV head and the key tile
-                        if (!ATTN_CHECK(st < static_cast<uint32_t>(C::STAGES) && zkv >= 0 && zkv < p.B * p.Hkv &&
-                                            j >= 0 && j * BN < p.Nk,
-                                        2u)) {
-                            ++kv_it;
-                            continue;
-                        }
-                        ptx::mbar_arrive_expect_tx_elect(bar(C::B_KVFULL + st), C::TILE_BYTES);
-                        const CUtensorMap *m = kv ? &tm_v : &tm_k;
+                // K (kv = 0) or V (kv = 1) of key tile j into the next ring stage
+                auto load_kv = [&](int j, int kv) -> bool {
+                    const uint32_t st = kv_it % C::STAGES;
+                    const uint32_t ph = ((kv_it / C::STAGES) & 1u) ^ 1u;
+                    if (!wait_warp(bar(C::B_KVEMPTY + st), ph, abort_flag, limit)) return false;
+                    ++kv_it;
+                    // debug build: the ring stage, the KV head and the key tile
+                    if (!ATTN_CHECK(st < static_cast<uint32_t>(C::STAGES) && zkv >= 0 && zkv < p.B * p.Hkv && j >= 0 &&
+                                        j * BN < p.Nk,
+                                    2u))
+                        return true;
+                    ptx::mbar_arrive_expect_tx_elect(bar(C::B_KVFULL + st), C::TILE_BYTES);
+                    const CUtensorMap *m = kv ? &tm_v : &tm_k;
 #pragma unroll
-                        for (int c = 0; c < C::NCHUNK; ++c)
-                            ptx::tma_load_3d_elect(sb + C::SMEM_KV + st * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                                   m, bar(C::B_KVFULL + st), c * C::CHUNK_COLS, j * BN, zkv);
-                        ++kv_it;
+                    for (int c = 0; c < C::NCHUNK; ++c)
+                        ptx::tma_load_3d_elect(sb + C::SMEM_KV + st * C::TILE_BYTES + c * C::CHUNK_BYTES, m,
+                                               bar(C::B_KVFULL + st), c * C::CHUNK_COLS, j * BN, zkv);
+                    return true;
+                };
+                if (DEC && p.dec2) {
+                    // both tiles on the split: key tiles in pairs, K K V V, in the order the
+                    // two tiles' products read them
+                    for (int j = lo0; ok && j < hi0; j += 2) {
+                        const bool two = j + 1 < hi0;
+                        ok = load_kv(j, 0);
+                        if (ok && two) ok = load_kv(j + 1, 0);
+                        if (ok) ok = load_kv(j, 1);
+                        if (ok && two) ok = load_kv(j + 1, 1);
+                    }
+                } else {
+                    for (int j = lo; ok && j < hi; ++j) {
+                        ok = load_kv(j, 0);  // K_j, then V_j
+                        if (ok) ok = load_kv(j, 1);
                     }
                 }
             }
@@ -594,6 +627,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tc_fence_after();
                 int prev = -1;
                 uint32_t vprev = 0, vprev_ph = 0;
+                if constexpr (DEC) {
+                    if (p.dec2) {
+                        // Decode shape, both tiles on the split's key tiles [lo0, hi0): tile 0
+                        // takes lo0, lo0 + 2, .., tile 1 lo0 + 1, lo0 + 3, .., both with the
+                        // one packed Q tile. The producer loads pairs of key tiles as K K V V.
+                        // A step issues both tiles' S and the previous step's P.V products;
+                        // every K and V tile has one reader and is released after it.
+                        const int a = lo0, bnd = hi0;
+                        const int n0 = (bnd - a + 1) / 2, n1 = (bnd - a) / 2;
+                        const uint32_t base = kv_it;
+                        kv_it += 2u * static_cast<uint32_t>(bnd - a);
+                        auto kv_index = [&](int j, uint32_t kv) -> uint32_t {
+                            const int r = j - a, pr = r >> 1, t = r & 1;
+                            const bool two = a + 2 * pr + 1 < bnd;
+                            return base + 4u * static_cast<uint32_t>(pr) +
+                                   (kv ? (two ? 2u + static_cast<uint32_t>(t) : 1u) : static_cast<uint32_t>(t));
+                        };
+                        auto kv_wait = [&](uint32_t it) -> bool {
+                            if (!wait_warp(bar(C::B_KVFULL + it % C::STAGES), (it / C::STAGES) & 1u, abort_flag, limit))
+                                return false;
+                            ptx::tc_fence_after();
+                            return true;
+                        };
+                        // S_t for key tile j (tile t's n-th), then K is released
+                        auto s_dec = [&](int t, int j) -> bool {
+                            const uint32_t it = kv_index(j, 0);
+                            if (!kv_wait(it)) return false;
+                            if constexpr (C::SEP_P) {
+                                uint32_t &sf = t ? sf_use1 : sf_use0;
+                                if (!wait_warp(bar(C::B_SFREE + t), (sf & 1u) ^ 1u, abort_flag, limit)) return false;
+                                ++sf;
+                                ptx::tc_fence_after();
+                            }
+                            issue_s(qa0, t ? C::COL_S1 : C::COL_S0, it % C::STAGES);
+                            ptx::mma_commit_elect(bar(C::B_SFULL + t));
+                            ptx::mma_commit_elect(bar(C::B_KVEMPTY + it % C::STAGES));
+                            return true;
+                        };
+                        // O_t (+)= P_t V for tile t's k-th key tile j; the last of the unit
+                        // reports O_t complete, the others (separate P) that P is free again
+                        auto pv_dec = [&](int t, int j, int k, bool last) -> bool {
+                            const uint32_t it = kv_index(j, 1);
+                            if (!kv_wait(it)) return false;
+                            uint32_t &pu = t ? p_use1 : p_use0;
+                            if (!issue_pv(t, t ? C::COL_O1 : C::COL_O0, t ? C::COL_P1 : C::COL_P0, it % C::STAGES, k > 0,
+                                          pu & 1u))
+                                return false;
+                            ++pu;
+                            if (last)
+                                ptx::mma_commit_elect(bar(C::B_OFULL + t));
+                            else if constexpr (C::SEP_P)
+                                ptx::mma_commit_elect(bar(C::B_PVDONE + t));
+                            ptx::mma_commit_elect(bar(C::B_KVEMPTY + it % C::STAGES));
+                            return true;
+                        };
+                        for (int st = 0; ok && st < n0; ++st) {
+                            const int j0 = a + 2 * st, j1 = j0 + 1;
+                            if constexpr (C::SEP_P) {
+                                ok = s_dec(0, j0);
+                                if (ok && st < n1) ok = s_dec(1, j1);
+                                if (ok && st > 0) ok = pv_dec(0, j0 - 2, st - 1, false);
+                                if (ok && st > 0 && st - 1 < n1) ok = pv_dec(1, j1 - 2, st - 1, st == n1);
+                            } else {
+                                if (st > 0) ok = pv_dec(0, j0 - 2, st - 1, false);
+                                if (ok) ok = s_dec(0, j0);
+                                if (ok && st > 0 && st - 1 < n1) ok = pv_dec(1, j1 - 2, st - 1, st == n1);
+                                if (ok && st < n1) ok = s_dec(1, j1);
+                            }
+                        }
+                        if (!ok) break;
+                        ptx::mma_commit_elect(bar(C::B_QEMPTY + qb));  // Q free once the last S is done
+                        // the last products: tile 0's always; tile 1's when it has as many key
+                        // tiles as tile 0 (with one fewer, its last came in the last step)
+                        ok = pv_dec(0, a + 2 * (n0 - 1), n0 - 1, true);
+                        if (ok && n1 > 0 && n1 == n0) ok = pv_dec(1, a + 2 * (n1 - 1) + 1, n1 - 1, true);
+                        if (!ok) break;
+                        continue;
+                    }
+                }
                 if constexpr (C::SEP_P) {
                     // S_t(j) is issued as soon as the softmax warps have read S_t(j-1);
                     // then come the P.V products of key tile j-1 for both query tiles.
@@ -795,11 +907,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t pv_w = 0;
         const uint32_t bar_p0 = bar(C::B_PFULL + 2 * t), bar_p1 = bar(C::B_PFULL + 2 * t + 1);
         const float sl2 = p.sl2;
-        uint32_t s_use = 0, o_use = 0;
+        uint32_t s_use = 0, o_use = 0, x_use = 0;
+        // decode with both tiles on a split: each tile takes every other key tile
+        const int jstep = (DEC && p.dec2) ? 2 : 1;
         bool ok = true;
         for (int k = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++k)) {
             const UnitInfo ui = unit_info<DEC>(u, p);
-            const int q0 = ui.q0a + t * BM;
+            // decode: tile 1 works only when both tiles share the split, on tile 0's rows
+            if (DEC && t == 1 && !p.dec2) continue;
+            const int q0 = ui.q0a + (DEC ? 0 : t * BM);
             if (q0 >= p.N) continue;  // no rows in this tile
             const int lo = t ? ui.lo1 : ui.lo0, hi = t ? ui.hi1 : ui.hi0;
             const int L = ui.L;
@@ -830,7 +946,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float m_run = -INFINITY;  // running max of scale*s*log2(e)
             float l_run = 0.f;        // running sum of 2^(x - m_run), for the LSE
             float r_run = 0.f;        // running sum of bf16(2^(x - m_run)), for normalising O
-            for (int j = lo; j < hi; ++j) {
+            for (int j = lo; j < hi; j += jstep) {
                 ok = wait_warp(bar_s, s_use & 1u, abort_flag, limit);
                 ++s_use;
                 if (!ok) break;
@@ -1009,6 +1125,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const size_t ridx = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
                                 static_cast<size_t>(qi);
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+            if constexpr (DEC) {
+                if (p.dec2) {
+                    // Tile 1 hands its normalised O and LSE to tile 0 through shared memory
+                    // (column by column: the 32 rows of a column are 32 consecutive floats);
+                    // tile 0 merges the two by log-sum-exp, as the split combine does, and
+                    // writes the result. The packed rows (at most 32) are the first warp's.
+                    if (quad != 0) continue;
+                    float *xo = reinterpret_cast<float *>(smem + C::SMEM_XCHG);
+                    float *xl = xo + 32 * D;
+                    if (t == 1) {
+                        ok = wait_warp(bar(C::B_XEMPTY), (x_use & 1u) ^ 1u, abort_flag, limit);
+                        ++x_use;
+                        if (!ok) break;
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t r[32];
+                            if (!empty) {
+                                ptx::tmem_ld32(t_o + 32 * c, r);
+                                ptx::tmem_wait_ld();
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) r[e] = 0u;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) xo[(32 * c + e) * 32 + lane] = __uint_as_float(r[e]) * inv_l;
+                        }
+                        xl[lane] = lse_nat;
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(C::B_XFULL));
+                        continue;
+                    }
+                    ok = wait_warp(bar(C::B_XFULL), x_use & 1u, abort_flag, limit);
+                    ++x_use;
+                    if (!ok) break;
+                    const float lse1 = xl[lane];
+                    const float mx2 = fmaxf(lse_nat, lse1);
+                    float w0 = 0.f, w1 = 0.f, lse_m = -INFINITY;
+                    if (mx2 != -INFINITY) {
+                        const float e0 = expf(lse_nat - mx2), e1 = expf(lse1 - mx2);
+                        w0 = e0 / (e0 + e1);
+                        w1 = e1 / (e0 + e1);
+                        lse_m = mx2 + logf(e0 + e1);
+                    }
+                    const size_t rows_out = static_cast<size_t>(p.B * p.Hkv) * static_cast<size_t>(p.N) *
+                                            static_cast<size_t>(p.splits > 1 ? p.splits : 1);
+                    const size_t prow = p.splits > 1 ? static_cast<size_t>(ui.split) * rows_per_split(p) + ridx : ridx;
+                    const bool store_row = qi < p.N && ATTN_CHECK(prow < rows_out, 10u);
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        if (!empty) {
+                            ptx::tmem_ld32(t_o + 32 * c, r);
+                            ptx::tmem_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) r[e] = 0u;
+                        }
+                        float v[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __uint_as_float(r[e]) * inv_l * w0 + xo[(32 * c + e) * 32 + lane] * w1;
+                        if (!store_row) continue;
+                        if (p.splits > 1) {
+                            float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D) + 8 * c;
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+                                dst[g] = make_float4(v[4 * g + 0], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D) + 4 * c;
+#pragma unroll
+                            for (int g = 0; g < 4; ++g)
+                                dst[g] = make_uint4(ptx::pack_bf16x2(v[8 * g + 0], v[8 * g + 1]),
+                                                    ptx::pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                                                    ptx::pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
+                                                    ptx::pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+                        }
+                    }
+                    if (store_row) (p.splits > 1 ? p.lse_part : p.lse)[prow] = lse_m;
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(C::B_XEMPTY));
+                    continue;
+                }
+            }
             // fp32 rows: the split results of the decode shape (merged later by the
             // combine kernel), or the plain forward's O when fp32 output was asked for.
             // The tensor-memory loads are warp-collective: every lane takes them, and
@@ -1282,7 +1481,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     if (!ATTN_CHECK(row >= 0 && splits >= 1, 30u)) return;
+    // the loads of different splits are independent: unrolled so that they overlap
     float m = -INFINITY;
+#pragma unroll 4
     for (int s = lane; s < splits; s += 32) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -1300,6 +1501,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
 #pragma unroll
     for (int c = 0; c < PER; ++c) acc[c] = 0.f;
     if (m != -INFINITY) {
+#pragma unroll 4
         for (int s = 0; s < splits; ++s) {
             const float l = lse_part[static_cast<size_t>(s) * rows + row];
             if (l == -INFINITY) continue;
@@ -1438,10 +1640,10 @@ int device_setup(int *sms_out) {
                                       Cfg<128>::SMEM_ALLOC)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      Cfg<64>::SMEM_ALLOC)) != cudaSuccess ||
+                                      Cfg<64, false, true>::SMEM_ALLOC)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      Cfg<128>::SMEM_ALLOC)) != cudaSuccess ||
+                                      Cfg<128, false, true>::SMEM_ALLOC)) != cudaSuccess ||
             (e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false, true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Cfg<128, true>::SMEM_ALLOC)) != cudaSuccess)
@@ -1544,6 +1746,7 @@ int launch(const void *q, const void *k, const void *v, void *o, float *o32, flo
     p.split_lo = p.split_len = p.split_hi = 0;
     p.div_splits = attn::make_fastdiv(1u);
     p.div_nq = attn::make_fastdiv(1u);
+    p.dec2 = 0;
     p.o_part = p.lse_part = nullptr;
     p.o32 = o32;
     p.q_scale = p.k_scale = p.v_scale = nullptr;
@@ -1592,6 +1795,7 @@ int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, 
     p.split_lo = p.split_len = p.split_hi = 0;
     p.div_splits = attn::make_fastdiv(1u);
     p.div_nq = attn::make_fastdiv(1u);
+    p.dec2 = 0;
     p.o_part = p.lse_part = nullptr;
     p.o32 = nullptr;
     p.q_scale = qs;
@@ -1742,6 +1946,10 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
     p.split_len = (p.split_hi - p.split_lo + splits - 1) / splits;
     p.div_splits = attn::make_fastdiv(static_cast<uint32_t>(splits));
     p.div_nq = attn::make_fastdiv(static_cast<uint32_t>(Nq));
+    // both query tiles on each split when the packed rows fit one warp's 32 lanes and the
+    // split is long enough (8 key tiles or more per tile) to pay for the exchange between
+    // the tiles at its end
+    p.dec2 = (R <= 32 && p.split_len >= 16) ? 1 : 0;
     p.num_units = static_cast<int>(bhkv * splits);
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     p.o32 = nullptr;
@@ -1753,7 +1961,8 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
         p.o_part = p.lse_part = nullptr;
     }
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
+    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D, false, true>::SMEM_ALLOC, stream>>>(
+        mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     if (splits > 1) {

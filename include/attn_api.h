@@ -147,7 +147,10 @@ int attn_fwd_o32(const void *q, const void *k, const void *v, float *o32, float 
  *
  * The G = Hq / Hkv query heads that share a KV head are packed into one tile of
  * G * Nq <= 128 rows (ATTN_ERR_UNSUPPORTED otherwise), so every K/V tile is read once
- * per split for all of them. ATTN_ERR_WORKSPACE when the workspace is too small.
+ * per split for all of them. With G * Nq <= 32 rows and 16 or more key tiles per split,
+ * both query tiles of a CTA work on one split, on alternate key tiles, and their results
+ * are merged in the CTA.
+ * ATTN_ERR_WORKSPACE when the workspace is too small.
  * Asynchronous on `stream`; calls that share a workspace must not overlap.
  */
 size_t attn_fwd_decode_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int splits);

@@ -82,3 +82,13 @@ def test_decode_workload_sampled():
     o_ref, l_ref = oracle.attn_ref_decode(q, k, v, causal=w.causal, scale=w.scale, rows=rows)
     compare(out.reshape(-1, w.d)[torch.from_numpy(rows).to(DEV)],
             lse.reshape(-1)[torch.from_numpy(rows).to(DEV)], o_ref, l_ref, "decode_8k")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nk,W,splits", [(3000, 2500, 1), (2200, 0, 1), (2048, 0, 1), (4500, 0, 2), (6200, 0, 3)])
+def test_decode_both_tiles_odd_and_even_tile_counts(Nk, W, splits, d):
+    # up to 32 packed rows and 16 or more key tiles per split put both query tiles on each
+    # split, alternating key tiles: splits of 20, 18, 16, 18 and 17 key tiles (odd and
+    # even counts, tile 1 ending a step before or with tile 0)
+    run_decode(2, 16, 2, 4, Nk, d, True, W, splits, seed=5600 + Nk + d + splits)
+    run_decode(2, 8, 2, 1, Nk, d, True, W, splits, seed=5700 + Nk + d + splits)
