@@ -9,8 +9,9 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO   (dK, dV summed over a group's heads)
 //
 // Three kernels:
-//   bwd_preprocess_kernel  per query row lse log2(e) and D = rowsum(dO o O) in fp32 (one
-//                          warp per row), each head's rows padded to a multiple of 128
+//   bwd_preprocess_kernel  per query row lse log2(e) and D = rowsum(dO o O) in fp32 (D / 8
+//                          lanes per row, several rows per warp), each head's rows padded
+//                          to a multiple of 128
 //   bwd kernel, MODE 0     key-stationary: a CTA holds K_j, V_j of one key tile and
 //                          streams (Q_i, dO_i) over every query head of the group and
 //                          every query tile that sees the keys: S^T = K Q^T and
@@ -79,46 +80,66 @@ struct BwdCfg {
 
 // Per query row of each head (N_pad rows, one warp each): lse log2(e) and
 // D = sum_c dO O in fp32; rows from N to N_pad get zeros.
+// Rows per warp of bwd_preprocess_kernel: a row is D / 8 lanes of 16 bytes, and each lane
+// keeps PRE_LOADS rows' loads in flight before reducing.
+constexpr int PRE_LOADS = 4;
+template <int D>
+__host__ __device__ constexpr int pre_rows_per_warp() { return PRE_LOADS * (32 / (D / 8)); }
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16 *__restrict__ o,
                                                              const __nv_bfloat16 *__restrict__ dout,
                                                              const float *__restrict__ lse,
                                                              float *__restrict__ lse2, float *__restrict__ dsum,
                                                              long long BH, int N, int N_pad) {
-    constexpr int PER = D / 32;  // bf16 per lane
-    const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    constexpr int LPR = D / 8;   // lanes per row, 8 bf16 (16 bytes) each
+    constexpr int RPL = 32 / LPR;  // rows per warp-wide load
+    constexpr int RPW = pre_rows_per_warp<D>();
+    static_assert(BM % RPW == 0, "a warp's rows lie in one head (N_pad is a multiple of BM)");
+    const long long prow0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW;
     const int lane = threadIdx.x & 31;
-    if (prow >= BH * N_pad) return;
-    if (!ATTN_CHECK(prow >= 0 && N <= N_pad, 25u)) return;
-    const long long h = prow / N_pad;
-    const int i = static_cast<int>(prow - h * N_pad);
-    if (i >= N) {
-        if (lane == 0) {
-            lse2[prow] = 0.f;
-            dsum[prow] = 0.f;
-        }
-        return;
-    }
-    const long long row = h * N + i;
-    const __nv_bfloat16 *a = o + row * D + lane * PER;
-    const __nv_bfloat16 *b = dout + row * D + lane * PER;
-    float acc = 0.f;
-    if constexpr (PER == 4) {
-        const uint2 x = *reinterpret_cast<const uint2 *>(a), y = *reinterpret_cast<const uint2 *>(b);
-        acc = fmaf(__uint_as_float(x.x << 16), __uint_as_float(y.x << 16), acc);
-        acc = fmaf(__uint_as_float(x.x & 0xFFFF0000u), __uint_as_float(y.x & 0xFFFF0000u), acc);
-        acc = fmaf(__uint_as_float(x.y << 16), __uint_as_float(y.y << 16), acc);
-        acc = fmaf(__uint_as_float(x.y & 0xFFFF0000u), __uint_as_float(y.y & 0xFFFF0000u), acc);
-    } else {
-        const uint32_t x = *reinterpret_cast<const uint32_t *>(a), y = *reinterpret_cast<const uint32_t *>(b);
-        acc = fmaf(__uint_as_float(x << 16), __uint_as_float(y << 16), acc);
-        acc = fmaf(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(y & 0xFFFF0000u), acc);
-    }
+    if (prow0 >= BH * N_pad) return;
+    if (!ATTN_CHECK(prow0 >= 0 && N <= N_pad && N_pad % RPW == 0, 25u)) return;
+    const long long h = prow0 / N_pad;
+    const int i0 = static_cast<int>(prow0 - h * N_pad);
+    const int sub = lane / LPR, part = lane - sub * LPR;
+    // every load first, then the products: PRE_LOADS independent 16-byte loads per operand
+    uint4 x[PRE_LOADS], y[PRE_LOADS];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        lse2[prow] = __ldg(lse + row) * 1.4426950408889634f;
-        dsum[prow] = acc;
+    for (int u = 0; u < PRE_LOADS; ++u) {
+        const int i = i0 + u * RPL + sub;
+        if (i < N) {
+            const long long off = (h * N + i) * D + part * 8;
+            x[u] = __ldg(reinterpret_cast<const uint4 *>(o + off));
+            y[u] = __ldg(reinterpret_cast<const uint4 *>(dout + off));
+        } else {
+            x[u] = make_uint4(0u, 0u, 0u, 0u);
+            y[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    float acc[PRE_LOADS];
+#pragma unroll
+    for (int u = 0; u < PRE_LOADS; ++u) {
+        const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w}, ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            a = fmaf(__uint_as_float(xs[e] << 16), __uint_as_float(ys[e] << 16), a);
+            a = fmaf(__uint_as_float(xs[e] & 0xFFFF0000u), __uint_as_float(ys[e] & 0xFFFF0000u), a);
+        }
+        // sum over the LPR lanes of the row (aligned groups of LPR lanes)
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        acc[u] = a;
+    }
+    if (part == 0) {
+#pragma unroll
+        for (int u = 0; u < PRE_LOADS; ++u) {
+            const int i = i0 + u * RPL + sub;
+            const long long prow = prow0 + u * RPL + sub;
+            lse2[prow] = i < N ? __ldg(lse + h * N + i) * 1.4426950408889634f : 0.f;
+            dsum[prow] = i < N ? acc[u] : 0.f;
+        }
     }
 }
 

@@ -2029,9 +2029,10 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     const int n_pad = static_cast<int>(bwd_n_pad(N));
     float *lse2 = static_cast<float *>(workspace);
     float *dsum = lse2 + BHq * n_pad;
-    // lse log2(e) and D = rowsum(dO o O), one warp per (padded) row
+    // lse log2(e) and D = rowsum(dO o O): warps of pre_rows_per_warp<D>() padded rows, 8 per block
     const long long prows = BHq * n_pad;
-    attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((prows + 7) / 8), 256, 0, stream>>>(
+    const long long pre_warps = prows / attn::pre_rows_per_warp<D>();
+    attn::bwd_preprocess_kernel<D><<<static_cast<unsigned>((pre_warps + 7) / 8), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse, lse2, dsum, BHq, N,
         n_pad);
     cudaError_t e = cudaGetLastError();
