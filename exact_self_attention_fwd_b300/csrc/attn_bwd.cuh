@@ -58,13 +58,17 @@ struct BwdCfg {
     static constexpr int HCHUNK_BYTES = CHUNK_BYTES / 2;       // 64 rows x 64 columns
     static constexpr int HTILE_BYTES = TILE_BYTES / 2;         // 64 rows x d
     static constexpr int HSTAGES = D == 64 ? 8 : 4;            // streamed half-tile pairs in flight
-    static constexpr int SMEM_FIX = 0;                         // the two stationary tiles
-    static constexpr int SMEM_RING = 2 * TILE_BYTES;           // HSTAGES x two streamed half tiles
+    // the two stationary tiles, in FIX_BUFS buffers: with two (d = 64, where shared memory
+    // has room), the producer loads the next unit's tiles while the current unit computes
+    static constexpr int FIX_BUFS = D == 64 ? 2 : 1;
+    static constexpr int SMEM_FIX = 0;
+    static constexpr int SMEM_RING = FIX_BUFS * 2 * TILE_BYTES;  // HSTAGES x two streamed half tiles
     static constexpr int SMEM_VEC = SMEM_RING + HSTAGES * 2 * HTILE_BYTES;  // per half-slot: lse2, D
     static constexpr int VEC_BYTES = 2 * 64 * 4;
     static constexpr int SMEM_BAR = SMEM_VEC + HSTAGES * VEC_BYTES;
-    static constexpr int B_FIXFULL = 0, B_FIXEMPTY = 1, B_FULL = 2, B_EMPTY = 2 + HSTAGES;
-    static constexpr int B_SDP = 2 + 2 * HSTAGES;  // 2: S and dP of sub-step h computed
+    static constexpr int B_FIXFULL = 0, B_FIXEMPTY = FIX_BUFS;  // FIX_BUFS each
+    static constexpr int B_FULL = 2 * FIX_BUFS, B_EMPTY = B_FULL + HSTAGES;
+    static constexpr int B_SDP = B_EMPTY + HSTAGES;  // 2: S and dP of sub-step h computed
     static constexpr int B_PDS = B_SDP + 2;        // 2: P (MODE 0) and dS of sub-step h written (4 warps)
     static constexpr int B_ACC = B_PDS + 2;        // accumulators of the unit complete
     static constexpr int B_AFREE = B_ACC + 1;      // accumulators read by the epilogue (8 warps)
@@ -259,8 +263,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(C::B_FIXFULL), 1);
-        ptx::mbar_init(bar(C::B_FIXEMPTY), 1);
+        for (int b = 0; b < C::FIX_BUFS; ++b) {
+            ptx::mbar_init(bar(C::B_FIXFULL + b), 1);
+            ptx::mbar_init(bar(C::B_FIXEMPTY + b), 1);
+        }
         for (int s = 0; s < C::HSTAGES; ++s) {
             ptx::mbar_init(bar(C::B_FULL + s), 1);
             ptx::mbar_init(bar(C::B_EMPTY + s), 1);
@@ -301,21 +307,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
             if (w.steps == 0) continue;
-            ok = wait_warp(bar(C::B_FIXEMPTY), (fix_it & 1u) ^ 1u, abort_flag, limit);
+            const uint32_t fb = fix_it % C::FIX_BUFS;
+            ok = wait_warp(bar(C::B_FIXEMPTY + fb), ((fix_it / C::FIX_BUFS) & 1u) ^ 1u, abort_flag, limit);
             ++fix_it;
             if (!ok) break;
+            const uint32_t fdst = sb + C::SMEM_FIX + fb * 2 * C::TILE_BYTES;
             // debug build: the stationary tile's head and rows
             if (!ATTN_CHECK(w.zfix >= 0 && w.zfix < p.B * (MODE == 0 ? p.Hkv : p.Hq) && w.tile >= 0 &&
                                 w.tile * BM < p.N,
                             20u))
                 continue;
-            ptx::mbar_arrive_expect_tx_elect(bar(C::B_FIXFULL), 2 * C::TILE_BYTES);
+            ptx::mbar_arrive_expect_tx_elect(bar(C::B_FIXFULL + fb), 2 * C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c) {
-                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + c * C::CHUNK_BYTES, &tm_fix0, bar(C::B_FIXFULL), c * 64,
+                ptx::tma_load_3d_elect(fdst + c * C::CHUNK_BYTES, &tm_fix0, bar(C::B_FIXFULL + fb), c * 64,
                                        w.tile * BM, w.zfix);
-                ptx::tma_load_3d_elect(sb + C::SMEM_FIX + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_fix1,
-                                       bar(C::B_FIXFULL), c * 64, w.tile * BM, w.zfix);
+                ptx::tma_load_3d_elect(fdst + C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_fix1, bar(C::B_FIXFULL + fb),
+                                       c * 64, w.tile * BM, w.zfix);
             }
             for (int s = 0; ok && s < w.steps; ++s) {
                 // MODE 0: step s = (head g of the group, query tile t); MODE 1: key tile t
@@ -362,7 +370,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const uint32_t last = (hit - 1u - slot) / C::HSTAGES * C::HSTAGES + slot;
                 drain_wait(bar(C::B_FULL + slot), (last / C::HSTAGES) & 1u, 100000000ull);
             }
-            if (fix_it) drain_wait(bar(C::B_FIXFULL), (fix_it - 1u) & 1u, 100000000ull);
+            for (uint32_t b = 0; b < static_cast<uint32_t>(C::FIX_BUFS); ++b) {
+                const uint32_t n_b = (fix_it + C::FIX_BUFS - 1u - b) / C::FIX_BUFS;  // loads into buffer b
+                if (n_b) drain_wait(bar(C::B_FIXFULL + b), (n_b - 1u) & 1u, 100000000ull);
+            }
         }
     } else if (warp == BWD_WARP_MMA) {
         // ================================================================ MMA issuer
@@ -432,11 +443,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
             if (w.steps == 0) continue;
-            ok = wait_warp(bar(C::B_FIXFULL), fix_use & 1u, abort_flag, limit);
+            const uint32_t fb = fix_use % C::FIX_BUFS;
+            ok = wait_warp(bar(C::B_FIXFULL + fb), (fix_use / C::FIX_BUFS) & 1u, abort_flag, limit);
             ++fix_use;
             if (!ok) break;
             ptx::tc_fence_after();
-            const uint32_t f0 = sb + C::SMEM_FIX, f1 = sb + C::SMEM_FIX + C::TILE_BYTES;
+            const uint32_t f0 = sb + C::SMEM_FIX + fb * 2 * C::TILE_BYTES, f1 = f0 + C::TILE_BYTES;
             uint32_t prev_slot = 0;
             for (int s = 0; s < w.steps; ++s) {
                 // order: S, dP of (s, 0); products of (s - 1, 1); S, dP of (s, 1); products
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (!ok) break;
             if (!(ok = issue_products(1, half_base(prev_slot), true))) break;
             ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
-            ptx::mma_commit_elect(bar(C::B_FIXEMPTY));
+            ptx::mma_commit_elect(bar(C::B_FIXEMPTY + fb));
             ptx::mma_commit_elect(bar(C::B_ACC));
         }
         ptx::mma_commit_elect(bar(C::B_DRAIN));
