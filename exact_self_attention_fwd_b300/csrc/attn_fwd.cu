@@ -167,7 +167,12 @@ struct Cfg {
     static constexpr int Q_BUFS = (D == 64 || F8) ? 2 : 1;
     static constexpr int SMEM_Q = 0;
     static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
+    // bf16 epilogue staging (plain forward at d = 128): 32 rows x 128 bytes per softmax
+    // warp, so that O leaves in whole 128-byte row pieces (see the epilogue)
+    static constexpr bool STAGE_O = !DEC && D == 128;
+    static constexpr int STG_BYTES = STAGE_O ? 8 * 32 * 128 : 0;
+    static constexpr int SMEM_STG = SMEM_KV + STAGES * TILE_BYTES;
+    static constexpr int SMEM_BAR = SMEM_STG + STG_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
     static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
@@ -1258,7 +1263,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // skipped). The tensor-memory loads are warp-collective, so every lane takes
             // them.
             const bool store_row = qi < p.N && ATTN_CHECK(ridx < rows_out, 7u);
-            {
+            if constexpr (C::STAGE_O) {
+                // Each thread's row in 16-byte pieces would make every store instruction
+                // touch 32 rows (32 partial sectors). Instead, for each 64-column (128-byte)
+                // piece of the rows, the warp's 32 rows go through its own staging block
+                // (16-byte units of row r at unit u ^ (r % 8), conflict-free both ways) and
+                // leave with 8 lanes per row: 4 whole 128-byte lines per instruction. (At
+                // d = 64, where a row is one such piece, the direct stores are as fast.)
+                const uint32_t stg = sb + C::SMEM_STG + static_cast<uint32_t>(warp) * 32u * 128u;
+                const uint32_t sw = static_cast<uint32_t>(lane & 7);
+                // the row this lane stores in round k: warp row (lane / 8) + 4k
+                const int rr0 = lane >> 3, part = lane & 7;
+                const size_t rbase = static_cast<size_t>(ui.zq) * static_cast<size_t>(p.N) +
+                                     static_cast<size_t>(q0 + quad * 32);
+#pragma unroll 1
+                for (int seg = 0; seg < D / 64; ++seg) {
+                    uint32_t r[2][32];
+                    if (!empty) {
+                        ptx::tmem_ld32(t_o + 64 * seg, r[0]);
+                        ptx::tmem_ld32(t_o + 64 * seg + 32, r[1]);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) r[h][e] = 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t *x = &r[u >> 2][8 * (u & 3)];
+                        uint4 val;
+                        val.x = ptx::pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
+                        val.y = ptx::pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+                        val.z = ptx::pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
+                        val.w = ptx::pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
+                        ptx::st_shared_v4(stg + static_cast<uint32_t>(lane) * 128u +
+                                              ((static_cast<uint32_t>(u) ^ sw) << 4),
+                                          val);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int kq = 0; kq < 8; ++kq) {
+                        const int wr = rr0 + 4 * kq;  // warp row
+                        const uint4 val = ptx::ld_shared_v4(stg + static_cast<uint32_t>(wr) * 128u +
+                                                            ((static_cast<uint32_t>(part) ^ static_cast<uint32_t>(wr & 7)) << 4));
+                        const size_t gidx = rbase + static_cast<size_t>(wr);
+                        if (q0 + quad * 32 + wr < p.N && ATTN_CHECK(gidx < rows_out, 7u))
+                            reinterpret_cast<uint4 *>(p.o + gidx * D + seg * 64)[part] = val;
+                    }
+                    __syncwarp();
+                }
+            } else {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + ridx * D);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
