@@ -407,6 +407,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // decode with splits: the merge kernel that follows may be scheduled now (it waits for
+    // this grid's completion before reading anything)
+    if constexpr (DEC) {
+        if (p.splits > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < C::Q_BUFS; ++b) {
@@ -1532,6 +1537,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float *__rest
                                                              float *__restrict__ lse, int rows,
                                                              int splits) {
     constexpr int PER = D / 32;
+    // launched as a programmatic dependent of the split kernel: the blocks may be resident
+    // before it ends; this waits until it has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x * 8 + static_cast<int>(threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -2021,11 +2029,22 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     if (splits > 1) {
-        const int blocks = static_cast<int>((rows + 7) / 8);
-        attn::decode_combine_kernel<D><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part,
-                                                                   static_cast<__nv_bfloat16 *>(o), lse,
-                                                                   static_cast<int>(rows), splits);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        // a programmatic dependent launch: its blocks can take SMs as split CTAs finish,
+        // instead of waiting for the whole grid to drain before being launched
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        lc.blockDim = dim3(256);
+        lc.dynamicSmemBytes = 0;
+        lc.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        la[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = la;
+        lc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&lc, attn::decode_combine_kernel<D>, static_cast<const float *>(p.o_part),
+                               static_cast<const float *>(p.lse_part), static_cast<__nv_bfloat16 *>(o), lse,
+                               static_cast<int>(rows), splits);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return ATTN_OK;
 }
