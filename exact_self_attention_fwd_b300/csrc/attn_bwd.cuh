@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     constexpr int RPL = 32 / LPR;  // rows per warp-wide load
     constexpr int RPW = pre_rows_per_warp<D>();
     static_assert(BM % RPW == 0, "a warp's rows lie in one head (N_pad is a multiple of BM)");
+    // the dK/dV kernel is launched as a programmatic dependent: it may be scheduled now
+    // and runs its prologue, then waits for this grid before reading the row terms
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long prow0 = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW;
     const int lane = threadIdx.x & 31;
     if (prow0 >= BH * N_pad) return;
@@ -295,6 +298,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
+    // Programmatic dependent launch: the prologue above may overlap the previous kernel
+    // of the pass; every read of the row terms (and of the inputs) comes after this wait
+    // for it to complete. The next kernel (dQ after dK/dV) may then be scheduled: it
+    // takes an SM as each CTA of this one exits.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     volatile uint32_t *abort_flag = &ctl->abort;
     const unsigned long long limit = p.timeout_ns;
     // half-slot n of the ring: streamed operand 0 at half_base(n), operand 1 HTILE_BYTES on

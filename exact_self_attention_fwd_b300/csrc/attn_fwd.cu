@@ -2139,15 +2139,26 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     // dK, dV: one unit per (key tile, batch, kv head)
     p.num_units = static_cast<int>(BHkv * p.n_kv);
     int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_bwd_kernel<D, 0><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mk, mv, mq64,
-                                                                                                  mdo64, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    // both kernels are programmatic dependents of the kernel before them (see the kernel's
+    // prologue): each starts its prologue while the previous one finishes
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc = {};
+    lc.blockDim = dim3(attn::BWD_THREADS);
+    lc.dynamicSmemBytes = attn::BwdCfg<D>::SMEM_ALLOC;
+    lc.stream = static_cast<cudaStream_t>(stream);
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    e = cudaLaunchKernelEx(&lc, attn::attn_bwd_kernel<D, 0>, mk, mv, mq64, mdo64, p);
+    if (e != cudaSuccess) return cuda_fail(e);
     // dQ: one unit per (query tile, batch, query head)
     p.num_units = static_cast<int>(BHq * p.n_kv);
     grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_bwd_kernel<D, 1><<<grid, attn::BWD_THREADS, attn::BwdCfg<D>::SMEM_ALLOC, stream>>>(mq, mdo, mk64,
-                                                                                                  mv64, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    e = cudaLaunchKernelEx(&lc, attn::attn_bwd_kernel<D, 1>, mq, mdo, mk64, mv64, p);
+    if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }
 
