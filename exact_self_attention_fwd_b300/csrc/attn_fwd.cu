@@ -390,6 +390,28 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const Params &p) {
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool DEC, bool F8>
+__global__ void attn_fwd_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                                const __grid_constant__ CUtensorMap, const Params);
+
+// Launches the forward kernel as a programmatic dependent of the previous kernel on the
+// stream (see the kernel's prologue).
+template <int D, bool DEC, bool F8>
+cudaError_t launch_fwd_kernel(int grid, size_t smem, cudaStream_t stream, const CUtensorMap &mq,
+                              const CUtensorMap &mk, const CUtensorMap &mv, const Params &p) {
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(NUM_THREADS);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, attn_fwd_kernel<D, DEC, F8>, mq, mk, mv, p);
+}
+
+template <int D, bool DEC, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -452,6 +474,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = ctl->tmem_base;
     volatile uint32_t *abort_flag = &ctl->abort;
     const unsigned long long limit = p.timeout_ns;
+    // Programmatic dependent launch: the prologue above may overlap the end of the kernel
+    // before this one on the stream (another attention call, say); every memory access
+    // of the pass comes after this wait for it to complete. A dependent launched after
+    // this kernel may be scheduled from now on; it waits likewise.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (!DEC) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp >= 8) {
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
@@ -1814,8 +1842,7 @@ int launch(const void *q, const void *k, const void *v, void *o, float *o32, flo
     p.o32 = o32;
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, false, false><<<grid, attn::NUM_THREADS, Cfg<D>::SMEM_ALLOC, stream>>>(mq, mk, mv, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = attn::launch_fwd_kernel<D, false, false>(grid, Cfg<D>::SMEM_ALLOC, stream, mq, mk, mv, p);
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }
@@ -1865,9 +1892,7 @@ int launch_fp8(const void *q8, const void *k8, const void *v8, const float *qs, 
     p.k_scale = ks;
     p.v_scale = vs;
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<128, false, true><<<grid, attn::NUM_THREADS, Cfg<128, true>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = attn::launch_fwd_kernel<128, false, true>(grid, Cfg<128, true>::SMEM_ALLOC, stream, mq, mk, mv, p);
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }
@@ -2024,9 +2049,7 @@ int launch_decode(const void *q, const void *k, const void *v, void *o, float *l
         p.o_part = p.lse_part = nullptr;
     }
     const int grid = p.num_units < sms ? p.num_units : sms;
-    attn::attn_fwd_kernel<D, true, false><<<grid, attn::NUM_THREADS, Cfg<D, false, true>::SMEM_ALLOC, stream>>>(
-        mq, mk, mv, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = attn::launch_fwd_kernel<D, true, false>(grid, Cfg<D, false, true>::SMEM_ALLOC, stream, mq, mk, mv, p);
     if (e != cudaSuccess) return cuda_fail(e);
     if (splits > 1) {
         // a programmatic dependent launch: its blocks can take SMs as split CTAs finish,
