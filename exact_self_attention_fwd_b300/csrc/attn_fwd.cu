@@ -1025,7 +1025,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // lo_max understate where some row's interval starts. (A third, all
                     // -inf branch for chunks outside every interval made the compiler
                     // spill the S registers.)
-                    const int lo_r = none ? BN : c_lo, hi_r = none ? -1 : c_hi;
+                    // A row past the tensor's end (q0 + row >= N: its output is never
+                    // stored) takes no part in the decision: it counts as the whole tile.
+                    // Rows inside N past a batch's key length must still come out as O = 0.
+                    const bool unstored = (DEC ? row : qi) >= p.N;
+                    const int lo_r = unstored ? 0 : (none ? BN : c_lo), hi_r = unstored ? BN - 1 : (none ? -1 : c_hi);
                     const int lo_max = __reduce_max_sync(0xffffffffu, lo_r);
                     const int hi_min = __reduce_min_sync(0xffffffffu, hi_r);
 #pragma unroll
