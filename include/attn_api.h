@@ -46,6 +46,13 @@
  *     memory is touched; the call then returns a negative attn_status and has no
  *     other effect. No error is fatal.
  *   - Calls on different streams, from different host threads, are safe.
+ *   - Stream order is kept. Each kernel is launched as a programmatic dependent of the
+ *     kernel before it on the stream: its prologue (barriers, tensor-memory allocation,
+ *     tensor-map prefetch) may run while that kernel finishes, but it touches no global
+ *     memory before that kernel has completed and its writes are visible
+ *     (griddepcontrol.wait). A kernel that follows one of these calls and was itself
+ *     launched with programmatic stream serialisation must wait likewise. Inside a CUDA
+ *     graph the same holds through programmatic dependency edges.
  */
 #ifndef ATTN_API_H
 #define ATTN_API_H
