@@ -151,8 +151,8 @@ struct Params {
 };
 
 // F8: Q, K and V are e4m3 codes (1 byte) instead of bf16 (2 bytes); O stays bf16.
-// DEC: the decode shape, which loads no Q for tile 1 and has room for a fifth stage at
-// d = 128.
+// DEC: the decode shape, which loads no Q for tile 1: its Q buffers have one slot, and at
+// d = 128 the ring has room for two more stages.
 template <int D, bool F8 = false, bool DEC = false>
 struct Cfg {
     static constexpr int ELEM = F8 ? 1 : 2;                 // bytes per Q/K/V element
@@ -161,18 +161,24 @@ struct Cfg {
     static constexpr int CHUNK_BYTES = BM * 128;            // one slab: 128 rows x 128 bytes
     static constexpr int NCHUNK = D / CHUNK_COLS;
     static constexpr int TILE_BYTES = CHUNK_BYTES * NCHUNK;
-    static constexpr int STAGES = (D == 128 && !F8) ? (DEC ? 5 : 4) : 8;
+    static constexpr int STAGES = (D == 128 && !F8) ? (DEC ? 6 : 4) : 8;
     // Q tiles of Q_BUFS units: with two, the producer loads the next unit's Q while the
     // current unit still computes (where shared memory has room for it).
     static constexpr int Q_BUFS = (D == 64 || F8) ? 2 : 1;
+    // Q tiles per buffer: the unit's two query tiles, or the decode shape's one packed tile
+    static constexpr int Q_SLOTS = DEC ? 1 : 2;
     static constexpr int SMEM_Q = 0;
-    static constexpr int SMEM_KV = Q_BUFS * 2 * TILE_BYTES;
+    static constexpr int SMEM_KV = Q_BUFS * Q_SLOTS * TILE_BYTES;
     // bf16 epilogue staging (plain forward at d = 128): 32 rows x 128 bytes per softmax
     // warp, so that O leaves in whole 128-byte row pieces (see the epilogue)
     static constexpr bool STAGE_O = !DEC && D == 128;
     static constexpr int STG_BYTES = STAGE_O ? 8 * 32 * 128 : 0;
     static constexpr int SMEM_STG = SMEM_KV + STAGES * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_STG + STG_BYTES;
+    // decode with both tiles on one split: tile 1's per-row factors for tile 0's merge,
+    // [2][32] floats (1 / sum of rounded P, and the LSE); its O stays in tensor memory
+    static constexpr int SMEM_XCHG = SMEM_STG + STG_BYTES;
+    static constexpr int XCHG_BYTES = DEC ? 2 * 32 * 4 : 0;
+    static constexpr int SMEM_BAR = SMEM_XCHG + XCHG_BYTES;
     // barrier indices
     static constexpr int B_QFULL = 0;                        // 2 * Q_BUFS: (buffer, tile)
     static constexpr int B_QEMPTY = 2 * Q_BUFS;              // Q_BUFS
@@ -183,8 +189,8 @@ struct Cfg {
     static constexpr int B_OFULL = B_PFULL + 4;     // 2
     static constexpr int B_SFREE = B_OFULL + 2;     // 2: softmax has read S_t (separate-P mode)
     static constexpr int B_PVDONE = B_SFREE + 2;    // 2: a P.V product of tile t completed
-    static constexpr int B_XFULL = B_PVDONE + 2;    // 1: decode, tile 1's result is in shared memory
-    static constexpr int B_XEMPTY = B_XFULL + 1;    // 1: decode, tile 0 has merged it
+    static constexpr int B_XFULL = B_PVDONE + 2;    // 1: decode, tile 1's factors are in shared memory
+    static constexpr int B_XEMPTY = B_XFULL + 1;    // 1: decode, tile 0 has read them and O_1
     static constexpr int B_DRAIN = B_XEMPTY + 1;    // 1
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
@@ -201,10 +207,6 @@ struct Cfg {
     static constexpr int P_COLS = BN * ELEM / 4;
     static constexpr uint32_t COL_P0 = SEP_P ? 256 + 2 * D : COL_S0;
     static constexpr uint32_t COL_P1 = SEP_P ? 256 + 2 * D + 64 : COL_S1;
-    // decode: tile 1's normalised O (fp32, [32][D]) and LSE ([32]) for tile 0 to merge,
-    // in the second Q slot of buffer 0, which the decode shape never loads
-    static constexpr int SMEM_XCHG = SMEM_Q + TILE_BYTES;
-    static_assert(!DEC || 32 * D * 4 + 32 * 4 <= TILE_BYTES, "decode exchange buffer");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = wait_warp(bar(C::B_QEMPTY + qb), qph ^ 1u, abort_flag, limit);
                 if (!ok) break;
                 ++q_it;
-                const uint32_t qdst = sb + C::SMEM_Q + qb * 2 * C::TILE_BYTES;
+                const uint32_t qdst = sb + C::SMEM_Q + qb * C::Q_SLOTS * C::TILE_BYTES;
                 // debug build: the Q buffer and the tensor-map z index of the unit's rows
                 if (!ATTN_CHECK(qb < static_cast<uint32_t>(C::Q_BUFS) && zq >= 0 &&
                                     zq < (DEC ? p.B * p.Hkv : p.B * p.Hq) && q0a >= 0 && q0a < p.N,
@@ -658,7 +660,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int hi = has1 ? max(hi0, hi1) : hi0;
                 const uint32_t qb = q_use % C::Q_BUFS, qph = (q_use / C::Q_BUFS) & 1u;
                 ++q_use;
-                const uint32_t qa0 = sb + C::SMEM_Q + qb * 2 * C::TILE_BYTES, qa1 = qa0 + C::TILE_BYTES;
+                // (the decode shape's tile 1 reads tile 0's packed Q)
+                const uint32_t qa0 = sb + C::SMEM_Q + qb * C::Q_SLOTS * C::TILE_BYTES;
+                const uint32_t qa1 = qa0 + (C::Q_SLOTS - 1) * C::TILE_BYTES;
                 ok = wait_warp(bar(C::B_QFULL + 2 * qb + 0), qph, abort_flag, limit);
                 if (ok) ok = wait_warp(bar(C::B_QFULL + 2 * qb + 1), qph, abort_flag, limit);
                 if (!ok) break;
@@ -1169,39 +1173,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float lse_nat = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
             if constexpr (DEC) {
                 if (p.dec2) {
-                    // Tile 1 hands its normalised O and LSE to tile 0 through shared memory
-                    // (column by column: the 32 rows of a column are 32 consecutive floats);
-                    // tile 0 merges the two by log-sum-exp, as the split combine does, and
-                    // writes the result. The packed rows (at most 32) are the first warp's.
+                    // Tile 1 hands tile 0 its rows' factors (1 / sum of rounded P, and the
+                    // LSE) through shared memory. Its O stays in tensor memory, where tile 0
+                    // reads it: the packed rows (at most 32) are the first warp's in both
+                    // tiles, so the same lanes hold them. Tile 0 merges the two by
+                    // log-sum-exp, as the split combine does, and writes the result. Tile 1's
+                    // first P.V product of its next unit overwrites O_1, so its warp goes on
+                    // only once tile 0 has read it.
                     if (quad != 0) continue;
-                    float *xo = reinterpret_cast<float *>(smem + C::SMEM_XCHG);
-                    float *xl = xo + 32 * D;
+                    float *xs = reinterpret_cast<float *>(smem + C::SMEM_XCHG);
                     if (t == 1) {
-                        ok = wait_warp(bar(C::B_XEMPTY), (x_use & 1u) ^ 1u, abort_flag, limit);
-                        ++x_use;
-                        if (!ok) break;
-#pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t r[32];
-                            if (!empty) {
-                                ptx::tmem_ld32(t_o + 32 * c, r);
-                                ptx::tmem_wait_ld();
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) r[e] = 0u;
-                            }
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) xo[(32 * c + e) * 32 + lane] = __uint_as_float(r[e]) * inv_l;
-                        }
-                        xl[lane] = lse_nat;
+                        xs[lane] = inv_l;
+                        xs[32 + lane] = lse_nat;
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(bar(C::B_XFULL));
+                        ok = wait_warp(bar(C::B_XEMPTY), x_use & 1u, abort_flag, limit);
+                        ++x_use;
+                        if (!ok) break;
                         continue;
                     }
                     ok = wait_warp(bar(C::B_XFULL), x_use & 1u, abort_flag, limit);
                     ++x_use;
                     if (!ok) break;
-                    const float lse1 = xl[lane];
+                    // tile 1 saw its last P.V product complete before it signalled
+                    ptx::tc_fence_after();
+                    const float inv_l1 = xs[lane], lse1 = xs[32 + lane];
+                    const bool empty1 = ui.hi1 <= ui.lo1;
+                    const uint32_t t_o1 = tmem + lane_off + C::COL_O1;
                     const float mx2 = fmaxf(lse_nat, lse1);
                     float w0 = 0.f, w1 = 0.f, lse_m = -INFINITY;
                     if (mx2 != -INFINITY) {
@@ -1216,18 +1214,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const bool store_row = qi < p.N && ATTN_CHECK(prow < rows_out, 10u);
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        if (!empty) {
-                            ptx::tmem_ld32(t_o + 32 * c, r);
-                            ptx::tmem_wait_ld();
-                        } else {
+                        uint32_t r[32], r1[32];
+                        if (!empty) ptx::tmem_ld32(t_o + 32 * c, r);
+                        if (!empty1) ptx::tmem_ld32(t_o1 + 32 * c, r1);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) r[e] = 0u;
+                        for (int e = 0; e < 32; ++e) {
+                            if (empty) r[e] = 0u;
+                            if (empty1) r1[e] = 0u;
                         }
                         float v[32];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = __uint_as_float(r[e]) * inv_l * w0 + xo[(32 * c + e) * 32 + lane] * w1;
+                        for (int e = 0; e < 32; ++e) {
+                            const float x1 = __uint_as_float(r1[e]) * inv_l1;
+                            v[e] = __uint_as_float(r[e]) * inv_l * w0 + x1 * w1;
+                        }
                         if (!store_row) continue;
                         if (p.splits > 1) {
                             float4 *dst = reinterpret_cast<float4 *>(p.o_part + prow * D) + 8 * c;
@@ -1245,6 +1246,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     if (store_row) (p.splits > 1 ? p.lse_part : p.lse)[prow] = lse_m;
+                    // O_1 has been read (and the factors): tile 1 may go on
+                    ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar(C::B_XEMPTY));
                     continue;
