@@ -70,14 +70,19 @@ struct BwdCfg {
     static constexpr int B_FULL = 2 * FIX_BUFS, B_EMPTY = B_FULL + HSTAGES;
     static constexpr int B_SDP = B_EMPTY + HSTAGES;  // 2: S and dP of sub-step h computed
     static constexpr int B_PDS = B_SDP + 2;        // 2: P (MODE 0) and dS of sub-step h written (4 warps)
-    static constexpr int B_ACC = B_PDS + 2;        // accumulators of the unit complete
-    static constexpr int B_AFREE = B_ACC + 1;      // accumulators read by the epilogue (8 warps)
-    static constexpr int B_DRAIN = B_AFREE + 1;
+    // accumulator sets: two where tensor memory has room (d = 64), so that a unit's
+    // products can start while the compute warps still have the previous unit's
+    // accumulators to read
+    static constexpr int ACC_BUFS = D == 64 ? 2 : 1;
+    static constexpr uint32_t ACC_COLS = 2 * D;   // dV and dK (MODE 0), or dQ (MODE 1)
+    static constexpr int B_ACC = B_PDS + 2;        // ACC_BUFS: accumulators of a unit complete
+    static constexpr int B_AFREE = B_ACC + ACC_BUFS;  // ACC_BUFS: read by the epilogue (8 warps)
+    static constexpr int B_DRAIN = B_AFREE + ACC_BUFS;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_ALLOC = SMEM_CTL + 16 + 1024;
     static constexpr uint32_t COL_BUF = 128;  // sub-step buffer h starts at column 128h
-    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_A0 = 256, COL_A1 = 256 + D;
+    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_A0 = 256, COL_A1 = 256 + D;  // set a: + a ACC_COLS
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
 };
@@ -278,8 +283,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_init(bar(C::B_SDP + h), 1);
             ptx::mbar_init(bar(C::B_PDS + h), 4);
         }
-        ptx::mbar_init(bar(C::B_ACC), 1);
-        ptx::mbar_init(bar(C::B_AFREE), 8);
+        for (int a = 0; a < C::ACC_BUFS; ++a) {
+            ptx::mbar_init(bar(C::B_ACC + a), 1);
+            ptx::mbar_init(bar(C::B_AFREE + a), 8);
+        }
         ptx::mbar_init(bar(C::B_DRAIN), 1);
         ctl->abort = 0u;
         ptx::fence_barrier_init();
@@ -427,17 +434,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         };
         // the accumulating products of sub-step h (half tile at hb), once the compute warps
         // wrote its P / dS
-        auto issue_products = [&](int h, uint32_t hb, bool accumulate) -> bool {
+        auto issue_products = [&](int h, uint32_t hb, bool accumulate, uint32_t acol) -> bool {
             uint32_t &use = h ? pds_use1 : pds_use0;
             if (!wait_warp(bar(C::B_PDS + h), use & 1u, abort_flag, limit)) return false;
             ++use;
             ptx::tc_fence_after();
             const uint32_t buf = C::COL_BUF * h;
             if constexpr (MODE == 0) {
-                issue_acc(C::COL_A0, buf + C::COL_S, hb + C::HTILE_BYTES, accumulate);  // dV += P^T dO
-                issue_acc(C::COL_A1, buf + C::COL_DP, hb, accumulate);                 // dK += dS^T Q
+                issue_acc(C::COL_A0 + acol, buf + C::COL_S, hb + C::HTILE_BYTES, accumulate);  // dV += P^T dO
+                issue_acc(C::COL_A1 + acol, buf + C::COL_DP, hb, accumulate);                 // dK += dS^T Q
             } else {
-                issue_acc(C::COL_A0, buf + C::COL_S, hb, accumulate);                  // dQ += dS K
+                issue_acc(C::COL_A0 + acol, buf + C::COL_S, hb, accumulate);                  // dQ += dS K
             }
             return true;
         };
@@ -458,6 +465,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t f0 = sb + C::SMEM_FIX + fb * 2 * C::TILE_BYTES, f1 = f0 + C::TILE_BYTES;
+            // this unit's accumulator set (units alternate between the sets)
+            const uint32_t aset = acc_fills % C::ACC_BUFS, aph = (acc_fills / C::ACC_BUFS) & 1u;
+            const uint32_t acol = aset * C::ACC_COLS;
+            ++acc_fills;
             uint32_t prev_slot = 0;
             for (int s = 0; s < w.steps; ++s) {
                 // order: S, dP of (s, 0); products of (s - 1, 1); S, dP of (s, 1); products
@@ -469,29 +480,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 if (!(ok = next_half(slot0))) break;
                 issue_sdp(0, f0, f1, half_base(slot0), half_base(slot0) + C::HTILE_BYTES);
                 if (s > 0) {
-                    if (!(ok = issue_products(1, half_base(prev_slot), true))) break;
+                    if (!(ok = issue_products(1, half_base(prev_slot), true, acol))) break;
                     ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
                 }
                 if (!(ok = next_half(slot1))) break;
                 issue_sdp(1, f0, f1, half_base(slot1), half_base(slot1) + C::HTILE_BYTES);
                 if (s == 0) {
-                    // the unit's first products overwrite the accumulators: both compute
-                    // warpgroups must have read the previous unit's (a fresh barrier
-                    // passes parity 1)
-                    ok = wait_warp(bar(C::B_AFREE), (acc_fills & 1u) ^ 1u, abort_flag, limit);
-                    ++acc_fills;
+                    // the unit's first products overwrite its accumulator set: both compute
+                    // warpgroups must have read what the unit ACC_BUFS back left there (a
+                    // fresh barrier passes parity 1)
+                    ok = wait_warp(bar(C::B_AFREE + aset), aph ^ 1u, abort_flag, limit);
                     if (!ok) break;
                     ptx::tc_fence_after();
                 }
-                if (!(ok = issue_products(0, half_base(slot0), s > 0))) break;
+                if (!(ok = issue_products(0, half_base(slot0), s > 0, acol))) break;
                 ptx::mma_commit_elect(bar(C::B_EMPTY + slot0));
                 prev_slot = slot1;
             }
             if (!ok) break;
-            if (!(ok = issue_products(1, half_base(prev_slot), true))) break;
+            if (!(ok = issue_products(1, half_base(prev_slot), true, acol))) break;
             ptx::mma_commit_elect(bar(C::B_EMPTY + prev_slot));
             ptx::mma_commit_elect(bar(C::B_FIXEMPTY + fb));
-            ptx::mma_commit_elect(bar(C::B_ACC));
+            ptx::mma_commit_elect(bar(C::B_ACC + aset));
         }
         ptx::mma_commit_elect(bar(C::B_DRAIN));
         drain_wait(bar(C::B_DRAIN), 0u, 100000000ull);
@@ -507,6 +517,66 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t t_dp = tmem + lane_off + C::COL_BUF * h + C::COL_DP;
         uint32_t hit = 0, sdp_use = 0, acc_use = 0;
         bool ok = true;
+        // Epilogue of a unit, split between the warpgroups: MODE 0 writes dV (warpgroup 0)
+        // and scale * dK (warpgroup 1) of the key rows; MODE 1 writes scale * dQ, columns
+        // [0, d/2) from warpgroup 0 and [d/2, d) from warpgroup 1. `fill` is the unit's
+        // index among those with something to stream (its accumulator set and phase); a
+        // unit with nothing to stream writes zeros.
+        auto epilogue = [&](int zfix, int r_row, bool has, uint32_t fill) -> bool {
+            const uint32_t aset = fill % C::ACC_BUFS;
+            if (has) {
+                if (!wait_warp(bar(C::B_ACC + aset), (fill / C::ACC_BUFS) & 1u, abort_flag, limit)) return false;
+                ptx::tc_fence_after();
+            }
+            __nv_bfloat16 *out = MODE == 0 ? (h == 0 ? p.dv : p.dk) : p.dq;
+            const float mul = (MODE == 0 && h == 0) ? 1.f : p.scale;
+            constexpr int NC = MODE == 0 ? D / 32 : D / 64;  // 32-column chunks this warpgroup writes
+            const int col0 = MODE == 0 ? 0 : h * (D / 2);
+            const uint32_t t_acc = tmem + lane_off + (MODE == 0 ? (h == 0 ? C::COL_A0 : C::COL_A1) : C::COL_A0) +
+                                   aset * C::ACC_COLS + col0;
+#pragma unroll 1
+            for (int c = 0; c < NC; ++c) {
+                uint32_t r[32];
+                if (has) {
+                    ptx::tmem_ld32(t_acc + 32 * c, r);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = 0u;
+                }
+                // debug build: the gradient row inside its output
+                if (r_row < p.N && ATTN_CHECK(zfix >= 0 && zfix < p.B * (MODE == 0 ? p.Hkv : p.Hq), 24u)) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(zfix) * p.N + r_row) * D + col0 +
+                                                           32 * c);
+#pragma unroll
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        uint4 val;
+                        val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 0]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 1]) * mul);
+                        val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 3]) * mul);
+                        val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 5]) * mul);
+                        val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * mul,
+                                                 __uint_as_float(r[8 * g4 + 7]) * mul);
+                        dst[g4] = val;
+                    }
+                }
+            }
+            if (has) {
+                // the accumulators are read: a later unit's first products may overwrite them
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_AFREE + aset));
+            }
+            return true;
+        };
+        // With two accumulator sets a unit's epilogue waits until this warpgroup has done
+        // its first sub-step of the next unit: the unit's last products then complete
+        // while the warps compute, instead of while they wait.
+        bool pend = false;
+        int pend_zfix = 0, pend_row = 0;
+        uint32_t pend_fill = 0;
         for (int kk = 0, u = snake_unit(0); ok && u < p.num_units; u = snake_unit(++kk)) {
             const BwdUnit w = bwd_unit<MODE>(u, p);
             const int r_abs = w.tile * BM + row;  // this thread's key (MODE 0) or query (MODE 1)
@@ -596,60 +666,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS + h));
+                if (C::ACC_BUFS > 1 && pend) {
+                    pend = false;
+                    if (!(ok = epilogue(pend_zfix, pend_row, true, pend_fill))) break;
+                }
             }
             if (!ok) break;
-            // epilogue, split between the warpgroups: MODE 0 writes dV (warpgroup 0) and
-            // scale * dK (warpgroup 1) of the key rows; MODE 1 writes scale * dQ, columns
-            // [0, d/2) from warpgroup 0 and [d/2, d) from warpgroup 1. A unit with nothing
-            // to stream writes zeros.
             const bool has = w.steps > 0;
-            if (has) {
-                ok = wait_warp(bar(C::B_ACC), acc_use & 1u, abort_flag, limit);
-                ++acc_use;
-                if (!ok) break;
-                ptx::tc_fence_after();
+            if (C::ACC_BUFS > 1 && pend) {
+                // (a unit with nothing to stream: the previous unit's epilogue first)
+                pend = false;
+                if (!(ok = epilogue(pend_zfix, pend_row, true, pend_fill))) break;
             }
-            __nv_bfloat16 *out = MODE == 0 ? (h == 0 ? p.dv : p.dk) : p.dq;
-            const float mul = (MODE == 0 && h == 0) ? 1.f : p.scale;
-            constexpr int NC = MODE == 0 ? D / 32 : D / 64;  // 32-column chunks this warpgroup writes
-            const int col0 = MODE == 0 ? 0 : h * (D / 2);
-            const uint32_t t_acc = tmem + lane_off + (MODE == 0 ? (h == 0 ? C::COL_A0 : C::COL_A1) : C::COL_A0) + col0;
-#pragma unroll 1
-            for (int c = 0; c < NC; ++c) {
-                uint32_t r[32];
-                if (has) {
-                    ptx::tmem_ld32(t_acc + 32 * c, r);
-                    ptx::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = 0u;
-                }
-                // debug build: the gradient row inside its output
-                if (r_abs < p.N && ATTN_CHECK(w.zfix >= 0 && w.zfix < p.B * (MODE == 0 ? p.Hkv : p.Hq), 24u)) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<size_t>(w.zfix) * p.N + r_abs) * D + col0 +
-                                                           32 * c);
-#pragma unroll
-                    for (int g4 = 0; g4 < 4; ++g4) {
-                        uint4 val;
-                        val.x = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 0]) * mul,
-                                                 __uint_as_float(r[8 * g4 + 1]) * mul);
-                        val.y = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 2]) * mul,
-                                                 __uint_as_float(r[8 * g4 + 3]) * mul);
-                        val.z = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 4]) * mul,
-                                                 __uint_as_float(r[8 * g4 + 5]) * mul);
-                        val.w = ptx::pack_bf16x2(__uint_as_float(r[8 * g4 + 6]) * mul,
-                                                 __uint_as_float(r[8 * g4 + 7]) * mul);
-                        dst[g4] = val;
-                    }
-                }
-            }
-            if (has) {
-                // the accumulators are read: the next unit's first products may overwrite them
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(C::B_AFREE));
+            const uint32_t fill = has ? acc_use++ : 0u;
+            if (has && C::ACC_BUFS > 1) {
+                pend = true;
+                pend_zfix = w.zfix;
+                pend_row = r_abs;
+                pend_fill = fill;
+            } else if (!(ok = epilogue(w.zfix, r_abs, has, fill))) {
+                break;
             }
         }
+        if (C::ACC_BUFS > 1 && ok && pend) ok = epilogue(pend_zfix, pend_row, true, pend_fill);
+        (void)ok;
     }
     ptx::tc_fence_before();
     __syncthreads();
