@@ -70,21 +70,27 @@ struct BwdCfg {
     static constexpr int B_FULL = 2 * FIX_BUFS, B_EMPTY = B_FULL + HSTAGES;
     static constexpr int B_SDP = B_EMPTY + HSTAGES;  // 2: S and dP of sub-step h computed
     static constexpr int B_PDS = B_SDP + 2;        // 2: P (MODE 0) and dS of sub-step h written (4 warps)
-    // accumulator sets: two where tensor memory has room (d = 64), so that a unit's
-    // products can start while the compute warps still have the previous unit's
-    // accumulators to read
-    static constexpr int ACC_BUFS = D == 64 ? 2 : 1;
-    static constexpr uint32_t ACC_COLS = 2 * D;   // dV and dK (MODE 0), or dQ (MODE 1)
-    static constexpr int B_ACC = B_PDS + 2;        // ACC_BUFS: accumulators of a unit complete
-    static constexpr int B_AFREE = B_ACC + ACC_BUFS;  // ACC_BUFS: read by the epilogue (8 warps)
-    static constexpr int B_DRAIN = B_AFREE + ACC_BUFS;
+    static constexpr int B_ACC = B_PDS + 2;        // 2: accumulators of a unit complete (per set)
+    static constexpr int B_AFREE = B_ACC + 2;      // 2: read by the epilogue (8 warps; per set)
+    static constexpr int B_DRAIN = B_AFREE + 2;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_CTL = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_ALLOC = SMEM_CTL + 16 + 1024;
     static constexpr uint32_t COL_BUF = 128;  // sub-step buffer h starts at column 128h
-    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_A0 = 256, COL_A1 = 256 + D;  // set a: + a ACC_COLS
+    static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_A0 = 256, COL_A1 = 256 + D;  // set a: + a BwdAcc::COLS
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory budget");
+};
+
+// Accumulator sets of a kernel: two where tensor memory has room beside the two sub-step
+// buffers (d = 64, and the dQ kernel, whose only accumulator is dQ), so that a unit's
+// products can start while the compute warps still have the previous unit's accumulators
+// to read; one for dK and dV at d = 128.
+template <int D, int MODE>
+struct BwdAcc {
+    static constexpr int BUFS = (D == 64 || MODE == 1) ? 2 : 1;
+    static constexpr uint32_t COLS = MODE == 0 ? 2 * D : D;  // dV and dK, or dQ
+    static_assert(256 + BUFS * COLS <= TMEM_COLS, "accumulator sets in tensor memory");
 };
 
 // Per query row of each head (N_pad rows, one warp each): lse log2(e) and
@@ -260,6 +266,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_str0, const __grid_constant__ CUtensorMap tm_str1,
                     const BwdParams p) {
     using C = BwdCfg<D>;
+    using A = BwdAcc<D, MODE>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_init(bar(C::B_SDP + h), 1);
             ptx::mbar_init(bar(C::B_PDS + h), 4);
         }
-        for (int a = 0; a < C::ACC_BUFS; ++a) {
+        for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar(C::B_ACC + a), 1);
             ptx::mbar_init(bar(C::B_AFREE + a), 8);
         }
@@ -466,8 +473,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t f0 = sb + C::SMEM_FIX + fb * 2 * C::TILE_BYTES, f1 = f0 + C::TILE_BYTES;
             // this unit's accumulator set (units alternate between the sets)
-            const uint32_t aset = acc_fills % C::ACC_BUFS, aph = (acc_fills / C::ACC_BUFS) & 1u;
-            const uint32_t acol = aset * C::ACC_COLS;
+            const uint32_t aset = acc_fills % A::BUFS, aph = (acc_fills / A::BUFS) & 1u;
+            const uint32_t acol = aset * A::COLS;
             ++acc_fills;
             uint32_t prev_slot = 0;
             for (int s = 0; s < w.steps; ++s) {
@@ -523,9 +530,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // index among those with something to stream (its accumulator set and phase); a
         // unit with nothing to stream writes zeros.
         auto epilogue = [&](int zfix, int r_row, bool has, uint32_t fill) -> bool {
-            const uint32_t aset = fill % C::ACC_BUFS;
+            const uint32_t aset = fill % A::BUFS;
             if (has) {
-                if (!wait_warp(bar(C::B_ACC + aset), (fill / C::ACC_BUFS) & 1u, abort_flag, limit)) return false;
+                if (!wait_warp(bar(C::B_ACC + aset), (fill / A::BUFS) & 1u, abort_flag, limit)) return false;
                 ptx::tc_fence_after();
             }
             __nv_bfloat16 *out = MODE == 0 ? (h == 0 ? p.dv : p.dk) : p.dq;
@@ -533,7 +540,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             constexpr int NC = MODE == 0 ? D / 32 : D / 64;  // 32-column chunks this warpgroup writes
             const int col0 = MODE == 0 ? 0 : h * (D / 2);
             const uint32_t t_acc = tmem + lane_off + (MODE == 0 ? (h == 0 ? C::COL_A0 : C::COL_A1) : C::COL_A0) +
-                                   aset * C::ACC_COLS + col0;
+                                   aset * A::COLS + col0;
 #pragma unroll 1
             for (int c = 0; c < NC; ++c) {
                 uint32_t r[32];
@@ -666,20 +673,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(C::B_PDS + h));
-                if (C::ACC_BUFS > 1 && pend) {
+                if (A::BUFS > 1 && pend) {
                     pend = false;
                     if (!(ok = epilogue(pend_zfix, pend_row, true, pend_fill))) break;
                 }
             }
             if (!ok) break;
             const bool has = w.steps > 0;
-            if (C::ACC_BUFS > 1 && pend) {
+            if (A::BUFS > 1 && pend) {
                 // (a unit with nothing to stream: the previous unit's epilogue first)
                 pend = false;
                 if (!(ok = epilogue(pend_zfix, pend_row, true, pend_fill))) break;
             }
             const uint32_t fill = has ? acc_use++ : 0u;
-            if (has && C::ACC_BUFS > 1) {
+            if (has && A::BUFS > 1) {
                 pend = true;
                 pend_zfix = w.zfix;
                 pend_row = r_abs;
@@ -688,7 +695,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 break;
             }
         }
-        if (C::ACC_BUFS > 1 && ok && pend) ok = epilogue(pend_zfix, pend_row, true, pend_fill);
+        if (A::BUFS > 1 && ok && pend) ok = epilogue(pend_zfix, pend_row, true, pend_fill);
         (void)ok;
     }
     ptx::tc_fence_before();
