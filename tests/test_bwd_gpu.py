@@ -174,6 +174,15 @@ def test_bwd_multi_tile():
     check_bwd(1, 2, 2, 1000, 64, False, 0, seed=5601)
 
 
+@pytest.mark.parametrize("d,Hkv", [(64, 8), (128, 2)])
+def test_bwd_many_units_per_cta_with_padding(d, Hkv):
+    """More units than SMs (320 dQ units; 320 dK/dV units at d = 64), so each CTA runs
+    several and alternates between its accumulator sets, with padded batches whose tiles
+    past their length have nothing to stream (those units write zeros between units that
+    accumulate)."""
+    check_bwd(8, 8, Hkv, 640, d, True, 0, seed=5900 + d, key_len=[640, 200, 0, 513, 128, 1, 640, 300])
+
+
 # ------------------------------------------------------------ GPU forward feeding the backward
 @pytest.mark.parametrize("case", [
     (1, 2, 2, 197, 64, False, 0, None),
