@@ -92,3 +92,13 @@ def test_decode_both_tiles_odd_and_even_tile_counts(Nk, W, splits, d):
     # even counts, tile 1 ending a step before or with tile 0)
     run_decode(2, 16, 2, 4, Nk, d, True, W, splits, seed=5600 + Nk + d + splits)
     run_decode(2, 8, 2, 1, Nk, d, True, W, splits, seed=5700 + Nk + d + splits)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_decode_both_tiles_several_units_per_cta(d, splits):
+    # 40 x 8 KV heads (x splits) units of 17 or 18 key tiles with both query tiles on each
+    # split: more units than SMs, so a CTA merges one unit's two tiles (tile 0 reading
+    # tile 1's O from tensor memory) and then runs the next unit, whose first P.V product
+    # overwrites that O
+    run_decode(40, 32, 8, 1, 2200 * splits, d, True, 0, splits, seed=5950 + d + splits)
